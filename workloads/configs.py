@@ -1,0 +1,78 @@
+"""The five synthetic decode workloads and a generic spec for test cases.
+
+Shapes follow the generation-phase decode problem described on the XQA page
+("TensorRT-LLM 源码完全拆解(二十九)", section on decode constraints), the MetaX
+grouped kernel PR (performance table: 32/4 heads, D=64, page 256, L=1536,
+split 8) and the FlashMLA walk-through (656-byte FP8 token, section
+"数据加载").
+"""
+from dataclasses import dataclass, field, replace
+from typing import Optional, Sequence
+
+# kv dtype tags (mirrors da_kv_dtype in include/decode_attn.h; plain ints so
+# that this module holds no dependency on the library)
+KV_BF16 = 0
+KV_FP8 = 1
+KV_MLA656 = 2
+
+
+@dataclass(frozen=True)
+class WorkloadSpec:
+    name: str
+    B: int
+    H_kv: int
+    G: int
+    D_qk: int
+    D_v: int
+    page_size: int
+    kv_dtype: int = KV_BF16
+    # sequence lengths: either a fixed list, or a distribution recipe
+    lengths: Optional[Sequence[int]] = None
+    length_dist: str = "fixed"          # fixed | uniform | loguniform
+    length_lo: int = 0
+    length_hi: int = 0
+    splits: int = 0                     # 0 = auto (balanced over SMs)
+    extra_pages: int = 0                # unused pages in the pool (poisoned)
+    softmax_scale: float = 0.0          # 0 = 1/sqrt(D_qk)
+    seed: int = 0
+    description: str = field(default="", compare=False)
+
+    @property
+    def H_q(self) -> int:
+        return self.H_kv * self.G
+
+    def with_(self, **kw) -> "WorkloadSpec":
+        return replace(self, **kw)
+
+
+CONFIGS = [
+    WorkloadSpec(
+        name="tiny_gqa_bf16", B=1, H_kv=1, G=8, D_qk=64, D_v=64, page_size=16,
+        lengths=[256], splits=1, extra_pages=48, seed=1000,
+        description="B=1 H_q=8 H_kv=1 D=64 L=256 P=16, 64-page pool, splits=1"),
+    WorkloadSpec(
+        name="gqa_bf16_b8", B=8, H_kv=4, G=8, D_qk=64, D_v=64, page_size=256,
+        lengths=[1536] * 8, splits=8, seed=1001,
+        description="B=8 H_q=32 H_kv=4 D=64 P=256 L=1536 splits=8 (MetaX shape, batch 8)"),
+    WorkloadSpec(
+        name="mixed_gqa_bf16", B=32, H_kv=8, G=8, D_qk=128, D_v=128, page_size=64,
+        length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1002,
+        description="B=32 H_q=64 H_kv=8 D=128 P=64 L~U[1024,8192] auto splits"),
+    WorkloadSpec(
+        name="fp8_gqa", B=64, H_kv=4, G=8, D_qk=128, D_v=128, page_size=32,
+        kv_dtype=KV_FP8, lengths=[32768] * 64, splits=0, seed=1003,
+        description="B=64 H_q=32 H_kv=4 D=128 P=32 L=32768 e4m3 KV, per-(head,tensor) fp32 scales"),
+    WorkloadSpec(
+        name="mla_fp8", B=32, H_kv=1, G=128, D_qk=576, D_v=512, page_size=64,
+        kv_dtype=KV_MLA656, length_dist="loguniform", length_lo=4096, length_hi=131072,
+        splits=0, seed=1004,
+        description="B=32 H_q=128 H_kv=1 D_qk=576 D_v=512 P=64 656-byte FP8 tokens, "
+                    "L log-uniform [4096,131072]"),
+]
+
+
+def spec_by_name(name: str) -> WorkloadSpec:
+    for s in CONFIGS:
+        if s.name == name:
+            return s
+    raise KeyError(name)
