@@ -315,3 +315,27 @@ def test_bad_page_id_is_reported(oracle_lib):
     w.block_table[0, 1] = w.num_pages + 5
     with pytest.raises(ValueError):
         oracle.attend(w)
+
+
+def test_query_head_order_h_times_g_plus_g(oracle_lib):
+    # query head h*G+g belongs to KV head h (XQA page, GQA layout section):
+    # give each global query head a one-hot query that selects its own token
+    spec = _small(B=1, lengths=[16], H_kv=3, G=2, D_qk=8, D_v=8, page_size=4)
+    w = make_workload(spec)
+    q = torch.zeros_like(w.q)
+    for hq in range(spec.H_q):
+        q[0, hq, hq] = 8.0
+    w.q = q
+    for h in range(spec.H_kv):
+        for t in range(16):
+            k = torch.zeros(8)
+            if t < spec.H_q:
+                k[t] = 64.0
+            _set_logical(w, 0, t, h, k=k.to(torch.bfloat16),
+                         v=_bf16([float(100 * h + t)] * 8))
+    out, _ = oracle.attend(w)
+    for h in range(spec.H_kv):
+        for g in range(spec.G):
+            hq = h * spec.G + g
+            assert torch.allclose(out[0, hq], torch.full((8,), float(100 * h + hq), dtype=torch.float64),
+                                  atol=1e-9, rtol=0)
