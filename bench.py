@@ -1,0 +1,419 @@
+"""Device-timed benchmark of paged-KV decode attention on GB300.
+
+One step = one pass of the whole hot path over one batch: the scheduling
+metadata kernel, the split-KV kernel and the LSE combine kernel. Inputs are
+seeded synthetic tensors resident in HBM before timing starts. Workloads whose
+KV is smaller than twice the L2 (129 MB) rotate through enough copies of the
+inputs that every step reads its KV from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica of the workload (the path shards by request / KV head
+with no exchange); value = all ranks' calls / max-over-ranks time.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_WORKLOAD = "gqa_bf16_b8"
+METRIC = "decode attn us/call (KV-read HBM GB/s, % of GB300 peak), device-timed"
+# the pages' own figure for this exact workload (MetaX C500, 25% compute slice, graph mode, batch 8)
+PAGE_NUMBERS_US = {"gqa_bf16_b8": 248.43}
+MAIN_KERNEL_SOURCES = {
+    "gqa": "paged_kv_cache_60_gb300/csrc/decode_gqa.cu",
+    "mla": "paged_kv_cache_60_gb300/csrc/decode_mla.cu",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--eager", action="store_true", help="launch every step from the host (no CUDA graph)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if n > 0 else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML every ~2 ms."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, bus_id):
+        self.samples, self.reasons, self.max_mhz, self.ok = [], 0, None, False
+        self._stop = threading.Event()
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            assert self.nvml.nvmlInit_v2() == 0
+            self.dev = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.dev)) != 0:
+                assert self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.dev)) == 0
+            m = ctypes.c_uint(0)
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(m))
+            self.max_mhz = m.value
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        mhz, r = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        get_r = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if get_r(self.dev, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(v for k, v in self.REASONS.items() if self.reasons & k),
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic(kernel_key, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (sha recorded in the summary)."""
+    src = os.path.join(ROOT, MAIN_KERNEL_SOURCES[kernel_key])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"{kernel_key}_decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for ln in open(path):
+        if ":" in ln and ln.startswith("- "):
+            k, v = ln[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def make_desc(da, w):
+    s = w.spec
+    return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,
+                        max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=s.kv_dtype,
+                        splits=s.splits, softmax_scale=s.softmax_scale)
+
+
+class DevCopy:
+    def __init__(self, torch, w, desc, da):
+        dev = "cuda"
+        self.q = w.q.to(dev)
+        self.k_pool = w.k_pool.to(dev)
+        self.v_pool = w.v_pool.to(dev) if w.v_pool is not None else None
+        self.k_scale = w.k_scale.to(dev) if w.k_scale is not None else None
+        self.v_scale = w.v_scale.to(dev) if w.v_scale is not None else None
+        self.block_table = w.block_table.to(dev)
+        self.cache_seqlens = w.cache_seqlens.to(dev)
+        s = w.spec
+        self.meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(s.B, s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(s.B, s.H_q, dtype=torch.float32, device=dev)
+
+    def step(self, da, desc, stream, **kw):
+        da.sched_meta(desc, self.cache_seqlens, self.meta, stream=stream)
+        da.fwd(desc, self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale, self.block_table,
+               self.cache_seqlens, self.meta, self.out, self.lse, stream=stream, **kw)
+
+
+def oracle_time_per_call(w, budget_s):
+    """Oracle (float64, host cores) on a bounded sample of (request, KV head)
+    units, scaled to one whole call. Returns (us_per_call, cores, sample text)."""
+    import oracle
+    s = w.spec
+    units_all = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
+    cost = {u: w.lengths[u[0]] for u in units_all}
+    total_cost = sum(cost.values())
+    # cheap probe on the shortest unit to size the sample
+    probe = min(units_all, key=lambda u: cost[u])
+    t0 = time.perf_counter()
+    oracle.attend(w, heads=[probe])
+    t_probe = max(time.perf_counter() - t0, 1e-6)
+    per_token = t_probe / max(1, cost[probe])
+    cores = oracle.num_threads()
+    # spread units in a fixed order, take a prefix until the budget is used
+    order = sorted(units_all, key=lambda u: (u[0] * 7919 + u[1] * 104729) % len(units_all))
+    sample, est = [], 0.0
+    for u in order:
+        sample.append(u)
+        est += per_token * cost[u] / max(1, min(cores, len(sample)))
+        if est >= budget_s:
+            break
+    reps = 1
+    t0 = time.perf_counter()
+    oracle.attend(w, heads=sample)
+    el = time.perf_counter() - t0
+    while el * (reps + 1) / reps < budget_s and reps < 1000:
+        oracle.attend(w, heads=sample)
+        reps += 1
+        el = time.perf_counter() - t0
+    sample_cost = sum(cost[u] for u in sample)
+    us = el / reps * (total_cost / sample_cost) * 1e6
+    text = (f"{len(sample)} of {len(units_all)} (request, KV head) units, {sample_cost} of {total_cost} "
+            f"tokens x heads, {reps} repetition(s), scaled to one whole call")
+    return us, cores, text
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from workloads import make_workload, spec_by_name
+    w = make_workload(spec_by_name(args.workload))
+    # each step times the oracle on a bounded sample; the whole run stays within a few minutes
+    budget = max(0.05, min(4.0, 150.0 / (args.steps + args.warmup + 1)))
+    oracle_time_per_call(w, budget)
+    times = []
+    cores, text = 0, ""
+    for _ in range(args.steps):
+        us, cores, text = oracle_time_per_call(w, budget)
+        times.append(us)
+    v = statistics.median(times)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "us/call", "n_gpus": args.gpus,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": round(v / 1000.0, 6),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "desc": w.spec.description},
+            "cpu_baseline": {"value": round(v, 3), "unit": "us/call", "cores": cores, "kind": "oracle",
+                             "sample": text},
+            "e2e": {"value": round(v, 3), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import paged_kv_cache_60_gb300 as da
+    from paged_kv_cache_60_gb300 import build as dabuild
+    from workloads import make_workload, spec_by_name
+
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        dabuild.build()
+    dist_barrier(world)
+    da.load_library()
+    spec = spec_by_name(args.workload)
+    w = make_workload(spec)
+    desc = make_desc(da, w)
+    kv_bytes = w.kv_bytes()
+    copies = 1 if kv_bytes >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / kv_bytes))
+    devs = [DevCopy(torch, w, desc, da) for _ in range(copies)]
+    stream = torch.cuda.Stream()
+    steps, warm = args.steps, max(3, args.warmup)
+    launches_per_step = 3
+
+    # ---- graphs (one per input copy), or eager
+    graphs = None
+    with torch.cuda.stream(stream):
+        for d in devs:
+            d.step(da, desc, stream)
+        torch.cuda.synchronize()
+        if not args.eager:
+            graphs = []
+            for d in devs:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    d.step(da, desc, stream)
+                graphs.append(g)
+        torch.cuda.synchronize()
+
+    def do_step(k):
+        if graphs is not None:
+            graphs[k % copies].replay()
+        else:
+            devs[k % copies].step(da, desc, stream)
+
+    bus = torch.cuda.get_device_properties(local)
+    bus_id = getattr(bus, "pci_bus_id", None)
+    bus_str = f"{getattr(bus, 'pci_domain_id', 0):08x}:{bus_id:02x}:{getattr(bus, 'pci_device_id', 0):02x}.0" \
+        if isinstance(bus_id, int) else ""
+
+    with torch.cuda.stream(stream):
+        for k in range(warm):
+            do_step(k)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(bus_str) as clk:
+            e0.record(stream)
+            for k in range(steps):
+                do_step(k)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        dist_barrier(world)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ms = dist_max(ms, world)
+    value_us = ms * 1000.0 / world     # whole-job: world replicas per step time
+    err = da.get_error(devs[0].meta, stream=stream)
+
+    # ---- dominant kernel: events around the split-KV kernel, every step (eager)
+    n_main = min(steps, 400)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_main)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        for k, (a, b) in enumerate(evs):
+            devs[k % copies].step(da, desc, stream, main_begin=a, main_end=b)
+        torch.cuda.synchronize()
+    main_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    peak, peak_kind = load_peaks()
+    achieved = kv_bytes / (main_ms * 1e-3) / 1e9
+    key = "mla" if spec.kv_dtype == da.KV_MLA656 else "gqa"
+    traffic = profile_traffic(key, args.workload)
+
+    # ---- end to end: host buffers in, host results out, every step
+    e2e = None
+    with torch.cuda.stream(stream):
+        host = {k: getattr(devs[0], k).cpu().pin_memory() for k in
+                ("q", "k_pool", "v_pool", "k_scale", "v_scale", "block_table", "cache_seqlens")
+                if getattr(devs[0], k) is not None}
+        h_out = torch.empty_like(devs[0].out, device="cpu").pin_memory()
+        h_lse = torch.empty_like(devs[0].lse, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+        n_e2e = max(3, min(steps, 50))
+
+        def e2e_step(k):
+            d = devs[k % copies]
+            for name, t in host.items():
+                getattr(d, name).copy_(t, non_blocking=True)
+            d.step(da, desc, stream)
+            h_out.copy_(d.out, non_blocking=True)
+            h_lse.copy_(d.lse, non_blocking=True)
+        for k in range(3):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(n_e2e):
+            e2e_step(k)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_us = a.elapsed_time(b) / n_e2e * 1000.0
+        e2e_us = dist_max(e2e_us, world) / world
+        e2e = {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, cores, text = oracle_time_per_call(w, 12.0)
+        cpu = {"value": round(us, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": text}
+
+    if rank == 0:
+        page = PAGE_NUMBERS_US.get(args.workload)
+        line = {
+            "metric": METRIC, "value": round(value_us, 4), "unit": "us/call", "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": round(ms, 6), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": round(value_us / page, 5) if page else None,
+            "dtype": "bf16" if spec.kv_dtype == da.KV_BF16 else "fp8-e4m3 kv / bf16 q,out",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "desc": spec.description, "B": spec.B, "H_q": spec.H_q,
+                       "H_kv": spec.H_kv, "D_qk": spec.D_qk, "D_v": spec.D_v, "page_size": spec.page_size,
+                       "splits": spec.splits, "kv_bytes_per_call": kv_bytes,
+                       "l2": ("inputs rotate over %d copies (%.0f MB > 2x L2)" % (copies, copies * kv_bytes / 1e6))
+                       if copies > 1 else "inputs larger than 2x L2",
+                       "launch": "eager" if args.eager else "cuda graph per step",
+                       "parallelism": f"replicas x{world}"},
+            "kv_read_gbs": round(kv_bytes / (ms * 1e-3) / 1e9 * world, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                         "kernel": f"{key}_decode_kernel", "main_kernel_us": round(main_ms * 1000.0, 3)},
+            "clocks": clk.summary(),
+            "gpu_launches": launches_per_step * steps,
+            "device_error": err,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * decode_attn.h -- C ABI of the paged-KV decode attention library (GB300, sm_103a).
+ *
+ * The operation (XQA page "TensorRT-LLM 源码完全拆解(二十九)", section
+ * "先把 decode 注意力的约束写清楚"): one new query token per request. For request
+ * b, KV head h and the G query heads h*G+g that share it,
+ *
+ *     out[b, h*G+g, :] = softmax(sigma * q[b, h*G+g, :] . K_{b,h}^T) V_{b,h}
+ *     lse[b, h*G+g]    = ln sum_t exp(sigma * q . k_t)           (natural log)
+ *
+ * where K_{b,h}, V_{b,h} are the first L_b = cache_seqlens[b] tokens of the
+ * request, gathered through block_table from a pool of fixed-size pages
+ * (XQA page, section "Hopper:一次 TMA 只搬一个页", "VLLM layout").
+ *
+ * The work is split along the sequence into split-KV partials, each with its
+ * own lse, and a combine step merges them (XQA page, section "归约怎么记";
+ * FlashMLA page "FlashMLA 注意力内核源码走读", sections "调度" and
+ * "合并与性能账本"). The call sequence follows FlashMLA's two-call shape:
+ *
+ *     decode_attn_sched_meta(...)   once per change of cache_seqlens (reusable)
+ *     decode_attn_fwd(...)          every decode step / layer
+ *
+ * Memory: the caller allocates every buffer. The library never allocates,
+ * never synchronises inside decode_attn_fwd, and keeps no per-call state
+ * outside the sched_meta buffer. All pointers below are DEVICE pointers unless
+ * noted; all must be 16-byte aligned.
+ *
+ * Errors: every entry point returns DA_OK (0) or a negative DA_ERR_* code,
+ * detected on the host before anything is launched. Errors that only the
+ * device can see (a block-table entry outside the pool, a length beyond
+ * max_pages_per_seq * page_size, a pipeline wait that ran out of time) set
+ * bits in an error word inside sched_meta; the kernels skip the offending
+ * work and never trap. Read the word with decode_attn_get_error.
+ *
+ * Determinism: identical inputs give bitwise identical out and lse (fixed
+ * reduction order, no floating-point atomics).
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* KV cache formats. */
+typedef enum {
+    /* k_pool, v_pool: bf16 [num_pages][page_size][H_kv][D], D = D_qk = D_v. */
+    DA_KV_BF16 = 0,
+    /* k_pool, v_pool: float8 e4m3 bytes [num_pages][page_size][H_kv][D];
+     * element value = e4m3 * k_scale[h] (resp. v_scale[h]), one fp32 scale per
+     * (KV head, tensor) -- the per-tensor KV scale of the XQA page, section
+     * "Hopper 路径上 V 不做显式反量化". */
+    DA_KV_FP8_PER_TENSOR = 1,
+    /* k_pool: 656-byte tokens [num_pages][page_size][1][656] (FlashMLA page,
+     * section "数据加载"): 512 e4m3, 4 fp32 scales (one per 128 values), 64 bf16
+     * RoPE values. K = the 576 dequantised values, V = the first 512. v_pool
+     * must be NULL or equal to k_pool; H_kv = 1, D_qk = 576, D_v = 512. */
+    DA_KV_FP8_MLA656 = 2
+} da_kv_dtype;
+
+/* Problem description (host struct, passed by pointer, not retained). */
+typedef struct {
+    int32_t B;                 /* requests */
+    int32_t H_kv;              /* KV heads */
+    int32_t G;                 /* query heads per KV head; H_q = H_kv * G */
+    int32_t D_qk;              /* q / K head size */
+    int32_t D_v;               /* V / out head size */
+    int32_t page_size;         /* tokens per page P: 8, 16, 32 or a multiple of 64 */
+    int32_t max_pages_per_seq; /* row length of block_table */
+    int32_t num_pages;         /* pages in the pool */
+    int32_t kv_dtype;          /* da_kv_dtype */
+    int32_t splits;            /* 0: balanced over the SMs; S > 0: S splits per request */
+    int32_t num_sms;           /* 0: query the current device */
+    float softmax_scale;       /* sigma; 0: 1/sqrt(D_qk) */
+} da_desc;
+
+/* Return codes. */
+#define DA_OK                  0
+#define DA_ERR_NULL           -1   /* a required pointer is NULL */
+#define DA_ERR_DIMS           -2   /* a size is out of range */
+#define DA_ERR_UNSUPPORTED    -3   /* no kernel for this (dtype, D_qk, D_v, G, page_size) */
+#define DA_ERR_ALIGN          -4   /* a pointer is not 16-byte aligned */
+#define DA_ERR_SPLITS         -5   /* splits < 0 or too large */
+#define DA_ERR_META_SIZE      -6   /* sched_meta buffer smaller than decode_attn_sched_meta_bytes */
+#define DA_ERR_CUDA           -7   /* a CUDA runtime/driver call failed */
+#define DA_ERR_SCALE          -8   /* FP8 format without k_scale / v_scale */
+
+/* Device error bits (sched_meta error word). */
+#define DA_DEV_BAD_PAGE        1   /* block_table entry outside [0, num_pages): page skipped */
+#define DA_DEV_SEQ_TOO_LONG    2   /* cache_seqlens[b] > max_pages_per_seq * page_size: clamped */
+#define DA_DEV_NEG_LEN         4   /* cache_seqlens[b] < 0: treated as 0 */
+#define DA_DEV_TIMEOUT         8   /* a pipeline wait ran out of time: work unit abandoned */
+#define DA_DEV_META_MISMATCH  16   /* sched_meta was built for another desc */
+
+/*
+ * Size in bytes of the sched_meta buffer for this desc (host only, no CUDA
+ * call except an SM-count query when desc->num_sms is 0). The buffer holds the
+ * scheduling metadata, the split-KV partials (fp32 o and lse per split and
+ * query head) and the device error word.
+ */
+int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
+
+/*
+ * Byte offsets inside sched_meta, for inspection and tests. offs[0..7] =
+ * header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part,
+ * total size. Header (16 int32): magic, B, H_kv, G, splits, num_parts, cpc,
+ * chunk (64), total_chunks, total_splits, per, error word, error detail,
+ * kv_dtype, num_sms, reserved. parts: num_parts records {b0, s0, c0, c1}
+ * (first request, its split index there, global chunk interval [c0, c1)).
+ * chunk_offset, split_offset: int32 [B+1] prefix sums; num_splits: int32 [B].
+ */
+int decode_attn_meta_offsets(const da_desc *desc, size_t offs[8]);
+
+/* Number of parts (grid x of the split-KV kernel) for this desc. */
+int decode_attn_num_parts(const da_desc *desc, int32_t *num_parts);
+
+/*
+ * Scheduling metadata (FlashMLA page, section "调度": a small kernel hands the
+ * (request, KV range) work units to the SMs ahead of time; the main kernel
+ * only reads them). Work is counted in chunks of 64 tokens.
+ *   splits = S > 0: request b is cut into S ranges of ceil(n_b / S) chunks
+ *     (FlashAttention tiling page, section 5.3, block.h split range);
+ *   splits = 0: all chunks of all requests are cut into
+ *     num_parts = floor(num_sms / (H_kv * cpc)) equal intervals, one per part.
+ * cache_seqlens: device int32 [B]. sched_meta: device, caller-owned, at least
+ * decode_attn_sched_meta_bytes. Launches one small kernel on `stream`; the
+ * result may be reused by any number of decode_attn_fwd calls while
+ * cache_seqlens and desc stay the same. Clears the device error word.
+ */
+int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
+                           void *sched_meta, size_t sched_meta_bytes, cudaStream_t stream);
+
+/*
+ * Decode attention forward. Launches the split-KV kernel and the LSE combine
+ * kernel (chained with programmatic dependent launch) on `stream`.
+ *   q:            bf16 [B][H_kv*G][D_qk], query head h*G+g belongs to KV head h
+ *   k_pool/v_pool: see da_kv_dtype
+ *   k_scale/v_scale: fp32 [H_kv] for DA_KV_FP8_PER_TENSOR, else ignored
+ *   block_table:  int32 [B][max_pages_per_seq]; entries past ceil(L_b/P) are never read
+ *   cache_seqlens: int32 [B] (must match what sched_meta was built from)
+ *   sched_meta:   from decode_attn_sched_meta; its partial buffers are overwritten,
+ *                 so two calls sharing one sched_meta must not overlap in time
+ *   out:          bf16 [B][H_kv*G][D_v]; lse: fp32 [B][H_kv*G]
+ * A request with L_b = 0 gets out = 0 and lse = -inf.
+ */
+int decode_attn_fwd(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                    const float *k_scale, const float *v_scale, const int32_t *block_table,
+                    const int32_t *cache_seqlens, void *sched_meta, size_t sched_meta_bytes,
+                    void *out, float *lse, cudaStream_t stream);
+
+/* Launch options for decode_attn_fwd_ex. */
+typedef struct {
+    int32_t use_pdl;          /* 1 (default behaviour of decode_attn_fwd): PDL-chain the kernels */
+    cudaEvent_t main_begin;   /* if not NULL: recorded on `stream` just before the split-KV kernel */
+    cudaEvent_t main_end;     /* if not NULL: recorded just after it (before the combine kernel) */
+} da_launch_opts;
+
+/* decode_attn_fwd with launch options (opts may be NULL). */
+int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                       const float *k_scale, const float *v_scale, const int32_t *block_table,
+                       const int32_t *cache_seqlens, void *sched_meta, size_t sched_meta_bytes,
+                       void *out, float *lse, const da_launch_opts *opts, cudaStream_t stream);
+
+/*
+ * Reads the device error word of sched_meta into *device_error (host int32).
+ * Synchronises `stream`.
+ */
+int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStream_t stream);
+
+/* Static description of a return code (never NULL). */
+const char *decode_attn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */

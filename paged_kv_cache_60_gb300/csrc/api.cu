@@ -1,0 +1,363 @@
+// Host side of the C ABI: argument checks, sched_meta layout, tensor maps,
+// kernel launches. No allocation, no synchronisation in the forward path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "decode_attn.h"
+#include "layout.h"
+
+namespace da {
+cudaError_t launch_sched_meta(const SchedParams &p, cudaStream_t stream, bool pdl);
+cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tk, const CUtensorMap &tv, const GqaParams &p,
+                       cudaStream_t stream, bool pdl);
+cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl);
+int mla_ctas_per_part();
+bool mla_kernel_available();
+}  // namespace da
+
+using namespace da;
+
+namespace {
+
+constexpr float kLog2eF = 1.4426950408889634f;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool is_mla(const da_desc *d) { return d->kv_dtype == DA_KV_FP8_MLA656; }
+
+// Which kernel serves this desc; returns DA_OK or an error code.
+int check_desc(const da_desc *d) {
+    if (!d) return DA_ERR_NULL;
+    if (d->B < 1 || d->B > (1 << 20) || d->H_kv < 1 || d->H_kv > 4096 || d->G < 1 || d->G > 1024 ||
+        d->page_size < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1 || d->D_qk < 1 || d->D_v < 1)
+        return DA_ERR_DIMS;
+    if ((int64_t)d->max_pages_per_seq * d->page_size > (int64_t)INT32_MAX - 64) return DA_ERR_DIMS;
+    if ((int64_t)d->B * d->max_pages_per_seq > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+    if (d->splits < 0 || d->splits > 4096) return DA_ERR_SPLITS;
+    if (d->num_sms < 0) return DA_ERR_DIMS;
+    if (!(d->softmax_scale >= 0.f) || std::isinf(d->softmax_scale)) return DA_ERR_DIMS;
+    const int P = d->page_size;
+    const bool page_ok = (P == 8 || P == 16 || P == 32 || (P % 64) == 0);
+    if (!page_ok) return DA_ERR_UNSUPPORTED;
+    switch (d->kv_dtype) {
+        case DA_KV_BF16:
+            if (d->G != 8 || d->D_qk != d->D_v || (d->D_qk != 64 && d->D_qk != 128)) return DA_ERR_UNSUPPORTED;
+            break;
+        case DA_KV_FP8_PER_TENSOR:
+            if (d->G != 8 || d->D_qk != 128 || d->D_v != 128) return DA_ERR_UNSUPPORTED;
+            break;
+        case DA_KV_FP8_MLA656:
+            if (d->H_kv != 1 || d->D_qk != 576 || d->D_v != 512 || d->G != 128) return DA_ERR_UNSUPPORTED;
+            if (!mla_kernel_available()) return DA_ERR_UNSUPPORTED;
+            break;
+        default:
+            return DA_ERR_UNSUPPORTED;
+    }
+    return DA_OK;
+}
+
+int resolve_sms(const da_desc *d, int *nsm) {
+    if (d->num_sms > 0) {
+        *nsm = d->num_sms;
+        return DA_OK;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DA_ERR_CUDA;
+    return DA_OK;
+}
+
+int cpc_of(const da_desc *d) { return is_mla(d) ? mla_ctas_per_part() : 1; }
+
+int make_layout(const da_desc *d, MetaLayout *L) {
+    int rc = check_desc(d);
+    if (rc) return rc;
+    int nsm = 0;
+    rc = resolve_sms(d, &nsm);
+    if (rc) return rc;
+    const int cpc = cpc_of(d);
+    int64_t num_parts, max_splits;
+    if (d->splits > 0) {
+        num_parts = (int64_t)d->B * d->splits;
+        max_splits = num_parts;
+    } else {
+        num_parts = nsm / (d->H_kv * cpc);
+        if (num_parts < 1) num_parts = 1;
+        max_splits = num_parts + d->B;
+    }
+    if (num_parts > (1 << 24)) return DA_ERR_SPLITS;
+    const int64_t H_q = (int64_t)d->H_kv * d->G;
+    size_t off = 0;
+    L->header = off;
+    off += kHeaderWords * 4;
+    L->parts = off;
+    off += round_up((size_t)num_parts * 16, 16);
+    L->chunk_offset = off;
+    off += round_up((size_t)(d->B + 1) * 4, 16);
+    L->split_offset = off;
+    off += round_up((size_t)(d->B + 1) * 4, 16);
+    L->num_splits = off;
+    off += round_up((size_t)d->B * 4, 16);
+    off = round_up(off, 256);
+    L->lse_part = off;
+    off += round_up((size_t)max_splits * H_q * 4, 256);
+    L->o_part = off;
+    off += round_up((size_t)max_splits * H_q * d->D_v * 4, 256);
+    L->total = off;
+    L->num_parts = (int32_t)num_parts;
+    L->max_splits = (int32_t)max_splits;
+    L->cpc = cpc;
+    return DA_OK;
+}
+
+MetaView meta_view(void *meta, const MetaLayout &L) {
+    uint8_t *base = static_cast<uint8_t *>(meta);
+    MetaView v;
+    v.header = reinterpret_cast<int32_t *>(base + L.header);
+    v.parts = reinterpret_cast<const int4 *>(base + L.parts);
+    v.chunk_offset = reinterpret_cast<const int32_t *>(base + L.chunk_offset);
+    v.split_offset = reinterpret_cast<const int32_t *>(base + L.split_offset);
+    v.num_splits = reinterpret_cast<const int32_t *>(base + L.num_splits);
+    v.lse_part = reinterpret_cast<float *>(base + L.lse_part);
+    v.o_part = reinterpret_cast<float *>(base + L.o_part);
+    v.max_splits = L.max_splits;
+    return v;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver at first use.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Pool [num_pages][P][H_kv][D] as a 4-D map; box = 128 bytes x 1 head x box_tok tokens x 1 page.
+int make_pool_map(CUtensorMap *m, const void *pool, const da_desc *d, int elem_bytes, int box_tok) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return DA_ERR_CUDA;
+    const int D = d->D_qk;
+    const cuuint64_t row = (cuuint64_t)D * elem_bytes;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)d->H_kv, (cuuint64_t)d->page_size, (cuuint64_t)d->num_pages};
+    cuuint64_t strides[3] = {row, row * d->H_kv, row * d->H_kv * d->page_size};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / elem_bytes), 1, (cuuint32_t)box_tok, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = enc(m, dt, 4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes) {
+    if (!bytes) return DA_ERR_NULL;
+    MetaLayout L;
+    const int rc = make_layout(desc, &L);
+    if (rc) return rc;
+    *bytes = L.total;
+    return DA_OK;
+}
+
+int decode_attn_meta_offsets(const da_desc *desc, size_t offs[8]) {
+    if (!offs) return DA_ERR_NULL;
+    MetaLayout L;
+    const int rc = make_layout(desc, &L);
+    if (rc) return rc;
+    offs[0] = L.header;
+    offs[1] = L.parts;
+    offs[2] = L.chunk_offset;
+    offs[3] = L.split_offset;
+    offs[4] = L.num_splits;
+    offs[5] = L.lse_part;
+    offs[6] = L.o_part;
+    offs[7] = L.total;
+    return DA_OK;
+}
+
+int decode_attn_num_parts(const da_desc *desc, int32_t *num_parts) {
+    if (!num_parts) return DA_ERR_NULL;
+    MetaLayout L;
+    const int rc = make_layout(desc, &L);
+    if (rc) return rc;
+    *num_parts = L.num_parts;
+    return DA_OK;
+}
+
+int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens, void *sched_meta,
+                           size_t sched_meta_bytes, cudaStream_t stream) {
+    MetaLayout L;
+    int rc = make_layout(desc, &L);
+    if (rc) return rc;
+    if (!cache_seqlens || !sched_meta) return DA_ERR_NULL;
+    if (!aligned16(sched_meta) || (reinterpret_cast<uintptr_t>(cache_seqlens) & 3u)) return DA_ERR_ALIGN;
+    if (sched_meta_bytes < L.total) return DA_ERR_META_SIZE;
+    int nsm = 0;
+    resolve_sms(desc, &nsm);
+    uint8_t *base = static_cast<uint8_t *>(sched_meta);
+    SchedParams p;
+    p.seqlens = cache_seqlens;
+    p.meta = reinterpret_cast<int32_t *>(base + L.header);
+    p.parts = reinterpret_cast<int32_t *>(base + L.parts);
+    p.chunk_offset = reinterpret_cast<int32_t *>(base + L.chunk_offset);
+    p.split_offset = reinterpret_cast<int32_t *>(base + L.split_offset);
+    p.num_splits = reinterpret_cast<int32_t *>(base + L.num_splits);
+    p.B = desc->B;
+    p.H_kv = desc->H_kv;
+    p.G = desc->G;
+    p.splits = desc->splits;
+    p.num_parts = L.num_parts;
+    p.cpc = L.cpc;
+    p.max_len = desc->max_pages_per_seq * desc->page_size;
+    p.kv_dtype = desc->kv_dtype;
+    p.num_sms = nsm;
+    if (launch_sched_meta(p, stream, true) != cudaSuccess) return DA_ERR_CUDA;
+    return DA_OK;
+}
+
+int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                       const float *k_scale, const float *v_scale, const int32_t *block_table,
+                       const int32_t *cache_seqlens, void *sched_meta, size_t sched_meta_bytes, void *out,
+                       float *lse, const da_launch_opts *opts, cudaStream_t stream) {
+    MetaLayout L;
+    int rc = make_layout(desc, &L);
+    if (rc) return rc;
+    const bool mla = is_mla(desc);
+    if (!q || !k_pool || !block_table || !cache_seqlens || !sched_meta || !out || !lse) return DA_ERR_NULL;
+    if (!mla && !v_pool) return DA_ERR_NULL;
+    if (mla && v_pool && v_pool != k_pool) return DA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool)) || !aligned16(block_table) ||
+        !aligned16(cache_seqlens) || !aligned16(sched_meta) || !aligned16(out) || !aligned16(lse))
+        return DA_ERR_ALIGN;
+    if (desc->kv_dtype == DA_KV_FP8_PER_TENSOR) {
+        if (!k_scale || !v_scale) return DA_ERR_SCALE;
+        if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+            return DA_ERR_ALIGN;
+    }
+    if (sched_meta_bytes < L.total) return DA_ERR_META_SIZE;
+    const bool pdl = opts ? opts->use_pdl != 0 : true;
+    const float sigma = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->D_qk);
+    const MetaView mv = meta_view(sched_meta, L);
+    const int H_q = desc->H_kv * desc->G;
+
+    if (opts && opts->main_begin && cudaEventRecord(opts->main_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
+    if (!mla) {
+        const bool fp8 = desc->kv_dtype == DA_KV_FP8_PER_TENSOR;
+        const int es = fp8 ? 1 : 2;
+        const int P = desc->page_size;
+        const int box_tok = P < kChunk ? P : kChunk;
+        CUtensorMap tk, tv;
+        if ((rc = make_pool_map(&tk, k_pool, desc, es, box_tok))) return rc;
+        if ((rc = make_pool_map(&tv, v_pool, desc, es, box_tok))) return rc;
+        GqaParams p;
+        p.q = q;
+        p.block_table = block_table;
+        p.seqlens = cache_seqlens;
+        p.k_scale = k_scale;
+        p.v_scale = v_scale;
+        p.meta = mv;
+        p.out = out;
+        p.lse = lse;
+        p.B = desc->B;
+        p.H_kv = desc->H_kv;
+        p.G = desc->G;
+        p.H_q = H_q;
+        p.max_pages = desc->max_pages_per_seq;
+        p.num_pages = desc->num_pages;
+        p.page_size = P;
+        p.box_tokens = box_tok;
+        p.boxes_per_chunk = kChunk / box_tok;
+        p.splits = desc->splits;
+        p.num_parts = L.num_parts;
+        p.scale_log2 = sigma * kLog2eF;
+        p.wait_limit_ns = kWaitLimitNs;
+        if (launch_gqa(desc->D_qk, fp8, tk, tv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
+    } else {
+        MlaParams p;
+        p.q = q;
+        p.pool = static_cast<const uint8_t *>(k_pool);
+        p.block_table = block_table;
+        p.seqlens = cache_seqlens;
+        p.meta = mv;
+        p.out = out;
+        p.lse = lse;
+        p.B = desc->B;
+        p.H_q = H_q;
+        p.max_pages = desc->max_pages_per_seq;
+        p.num_pages = desc->num_pages;
+        p.page_size = desc->page_size;
+        p.splits = desc->splits;
+        p.num_parts = L.num_parts;
+        p.scale_log2 = sigma * kLog2eF;
+        p.wait_limit_ns = kWaitLimitNs;
+        if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
+    }
+    if (opts && opts->main_end && cudaEventRecord(opts->main_end, stream) != cudaSuccess) return DA_ERR_CUDA;
+    CombineParams c;
+    c.meta = mv;
+    c.out = out;
+    c.lse = lse;
+    c.B = desc->B;
+    c.H_q = H_q;
+    c.D_v = desc->D_v;
+    c.H_kv = desc->H_kv;
+    c.G = desc->G;
+    c.splits = desc->splits;
+    c.num_parts = L.num_parts;
+    if (launch_combine(desc->D_v, c, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
+    return DA_OK;
+}
+
+int decode_attn_fwd(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                    const float *k_scale, const float *v_scale, const int32_t *block_table,
+                    const int32_t *cache_seqlens, void *sched_meta, size_t sched_meta_bytes, void *out, float *lse,
+                    cudaStream_t stream) {
+    return decode_attn_fwd_ex(desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seqlens, sched_meta,
+                              sched_meta_bytes, out, lse, nullptr, stream);
+}
+
+int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStream_t stream) {
+    if (!sched_meta || !device_error) return DA_ERR_NULL;
+    if (!aligned16(sched_meta)) return DA_ERR_ALIGN;
+    const int32_t *w = static_cast<const int32_t *>(sched_meta) + kHError;
+    if (cudaMemcpyAsync(device_error, w, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return DA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DA_ERR_CUDA;
+    return DA_OK;
+}
+
+const char *decode_attn_strerror(int code) {
+    switch (code) {
+        case DA_OK: return "ok";
+        case DA_ERR_NULL: return "a required pointer is NULL";
+        case DA_ERR_DIMS: return "a size is out of range";
+        case DA_ERR_UNSUPPORTED: return "no kernel for this (kv dtype, D_qk, D_v, G, page_size)";
+        case DA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case DA_ERR_SPLITS: return "splits out of range";
+        case DA_ERR_META_SIZE: return "sched_meta buffer too small";
+        case DA_ERR_CUDA: return "a CUDA call failed";
+        case DA_ERR_SCALE: return "FP8 KV needs k_scale and v_scale";
+        default: return "unknown error code";
+    }
+}
+
+}  // extern "C"

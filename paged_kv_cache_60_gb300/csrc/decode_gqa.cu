@@ -1,0 +1,534 @@
+// Split-KV decode kernel for grouped-query attention with G = 8 query heads
+// per KV head (bf16 KV with D = 64 / 128, e4m3 KV with D = 128).
+//
+// One CTA per (part, KV head). A part is a list of (request, chunk range)
+// segments from the scheduling metadata; a chunk is 64 tokens.
+//
+// Data path (XQA page "TensorRT-LLM 源码完全拆解(二十九)"):
+//  * page gather: one 4-D tensor map describes the whole pool
+//    [num_pages][P][H_kv][D]; the page id is the outermost TMA coordinate
+//    (section "Hopper:一次 TMA 只搬一个页"). Page ids are read by the producer
+//    warp 32 at a time, one per lane, and broadcast with shuffles, ahead of use.
+//  * K/V streaming: a producer warp fills an NS-stage ring of shared-memory
+//    stages (K tile + V tile of one chunk) with TMA; full/empty mbarriers hand
+//    stages to the consumer warps. Loads carry an L2 evict-first hint
+//    (FlashMLA page, section "数据加载": KV is streamed once).
+//  * the G query rows of one KV head stay in registers for the whole part, so
+//    each KV byte is read from HBM once per group (XQA page, section
+//    "GQA 的组内复用").
+//  * products: the KV tile sits on the M side of a 16x8x16 warp MMA and the
+//    G = 8 query heads on the N side -- the SWAP_AB orientation of the XQA page
+//    (section "SWAP_AB:把 K 放在 A 位"): S^T = K Q^T, O^T += V^T P^T. With G = 8
+//    the N = 8 side is exactly filled. P goes from the S accumulator to the PV
+//    operand through movmatrix (8x8 transpose in registers).
+//  * online softmax (attention pipeline page, section 三): running max m,
+//    running sum l, rescale alpha = 2^(m_old - m_new), exponentials by exp2
+//    with log2(e) folded into the score scale (same page, section 一).
+//  * FP8 KV: e4m3 stays e4m3 in shared memory and is widened to f16 in
+//    registers right before the MMA (XQA page, section "为什么不在搬入 SMEM 时就转换"),
+//    two values per cvt; the per-tensor scales are folded into the score scale
+//    (k_scale) and into the output (v_scale) (same page, section
+//    "Hopper 路径上 V 不做显式反量化").
+//  * every consumer warp owns 16 tokens of a chunk and keeps its own
+//    (m, l, O) state; at the end of a segment the warps' states are merged
+//    through shared memory in a fixed order, and the segment's result is
+//    written either as the final bf16 output (request has one split) or as a
+//    float32 partial plus its lse for the combine kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "decode_attn.h"
+
+namespace da {
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, bool FP8>
+struct GqaCfg {
+    static constexpr int G = 8;
+    static constexpr int ES = FP8 ? 1 : 2;
+    static constexpr int ROW = D * ES;       // bytes of one token's head
+    static constexpr int NX = ROW / 128;     // 128-byte TMA boxes per row
+    static constexpr int XBOX = 128 / ES;    // elements per box row
+    static constexpr int TILE = kChunk * ROW;
+    static constexpr int XTILE = kChunk * 128;  // one x-box column of a tile
+    static constexpr int STAGE = 2 * TILE;
+    static constexpr int NCW = 8;            // consumer warps
+    static constexpr int NGRP = NCW / 4;     // consumer groups (alternate chunks)
+    static constexpr int NS = FP8 ? 8 : (D == 128 ? 5 : 4);
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int MT = D / 16;
+    static constexpr int KS = D / 16;
+    static constexpr int UPAD = D + 4;
+    static constexpr int OFF_U = NS * STAGE;
+    static constexpr int OFF_M = OFF_U + NCW * G * UPAD * 4;
+    static constexpr int OFF_L = OFF_M + NCW * G * 4;
+    static constexpr int OFF_W = OFF_L + NCW * G * 4;
+    static constexpr int OFF_FIN = OFF_W + NCW * G * 4;
+    static constexpr int OFF_BAR = (OFF_FIN + 2 * G * 4 + 7) / 8 * 8;
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
+    static constexpr int MIN_BLOCKS = (D == 64 && !FP8) ? 2 : 1;
+    static_assert(ROW % 128 == 0, "rows must be whole 128-byte boxes");
+    static_assert(!FP8 || NX == 1, "fp8 path expects one 128-byte box per row");
+};
+
+// Walks the (request, split, local chunk range) segments of one part.
+struct SegWalker {
+    const int32_t *chunk_offset;
+    int B, b, s, c, c1;
+    bool pending_empty;
+    __device__ bool next(int &sb, int &ss, int &lc0, int &lc1) {
+        if (pending_empty) {
+            pending_empty = false;
+            sb = b;
+            ss = s;
+            lc0 = lc1 = c - chunk_offset[b];
+            c = c1;
+            return true;
+        }
+        if (b < 0 || c >= c1) return false;
+        while (b < B && chunk_offset[b + 1] <= c) {
+            ++b;
+            s = 0;
+        }
+        if (b >= B) return false;
+        const int end = min(c1, chunk_offset[b + 1]);
+        sb = b;
+        ss = s;
+        lc0 = c - chunk_offset[b];
+        lc1 = end - chunk_offset[b];
+        c = end;
+        ++b;
+        s = 0;
+        return true;
+    }
+};
+
+__device__ __forceinline__ SegWalker make_walker(const MetaView &mv, int part, int B) {
+    int4 r = mv.parts[part];
+    if (r.x >= B || r.z > r.w) r.x = -1;  // not a record this desc can produce
+    SegWalker w;
+    w.chunk_offset = mv.chunk_offset;
+    w.B = B;
+    w.b = r.x;
+    w.s = r.y;
+    w.c = r.z;
+    w.c1 = r.w;
+    w.pending_empty = (r.x >= 0) && (r.z == r.w);
+    return w;
+}
+
+__device__ __forceinline__ uint32_t keep_tokens(uint32_t x, int t_even, int nvalid) {
+    const uint32_t lo = (t_even < nvalid) ? 0x0000ffffu : 0u;
+    const uint32_t hi = (t_even + 1 < nvalid) ? 0xffff0000u : 0u;
+    return x & (lo | hi);
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_BLOCKS)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ GqaParams p) {
+    using C = GqaCfg<D, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *sm_u = reinterpret_cast<float *>(smem + C::OFF_U);
+    float *sm_m = reinterpret_cast<float *>(smem + C::OFF_M);
+    float *sm_l = reinterpret_cast<float *>(smem + C::OFF_L);
+    float *sm_w = reinterpret_cast<float *>(smem + C::OFF_W);
+    float *sm_fin = reinterpret_cast<float *>(smem + C::OFF_FIN);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *empty = full + C::NS;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int part = blockIdx.x, h = blockIdx.y;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == C::NCW && lane == 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    {
+        const int32_t *hd = p.meta.header;
+        const bool ok = hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv &&
+                        hd[kHG] == p.G && hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts &&
+                        (int)gridDim.x == p.num_parts;
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(&p.meta.header[kHError], DA_DEV_META_MISMATCH);
+            return;
+        }
+    }
+    const int max_len = p.max_pages * p.page_size;
+
+    if (warp == C::NCW) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = policy_evict_first();
+        SegWalker wk = make_walker(p.meta, part, p.B);
+        int i = 0;
+        bool aborted = false;
+        int sb, ss, lc0, lc1;
+        while (!aborted && wk.next(sb, ss, lc0, lc1)) {
+            if (lc0 == lc1) continue;
+            const int L = min(max(p.seqlens[sb], 0), max_len);
+            const int nb = p.boxes_per_chunk, bt = p.box_tokens;
+            const int total_boxes = (lc1 - lc0) * nb;
+            const int tok_base = lc0 * kChunk;
+            const int32_t *bt_row = p.block_table + (size_t)sb * p.max_pages;
+            auto page_of = [&](int gb) -> int {
+                const int tok = tok_base + gb * bt;
+                if (gb >= total_boxes || tok >= L) return -1;
+                return bt_row[tok / p.page_size];
+            };
+            int cur = page_of(lane), nxt = page_of(32 + lane), cur_base = 0;
+            for (int lc = lc0; lc < lc1; ++lc, ++i) {
+                const int stage = i % C::NS;
+                const uint32_t par = ((i / C::NS) & 1) ^ 1;
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait_bounded(&empty[stage], par, abort_flag, p.wait_limit_ns);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    aborted = true;
+                    break;
+                }
+                const int tok0 = lc * kChunk;
+                int pages[8];
+                uint32_t bytes = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    pages[j] = -1;
+                    if (j < nb) {
+                        const int gb = (lc - lc0) * nb + j;
+                        if (gb - cur_base >= 32) {
+                            cur = nxt;
+                            cur_base += 32;
+                            nxt = page_of(cur_base + 32 + lane);
+                        }
+                        const int pg = __shfl_sync(0xffffffffu, cur, gb - cur_base);
+                        if (tok0 + j * bt < L) {
+                            if (pg < 0 || pg >= p.num_pages) {
+                                if (lane == 0) {
+                                    atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
+                                    p.meta.header[kHErrorDetail] = pg;
+                                }
+                            } else {
+                                pages[j] = pg;
+                                bytes += 2u * C::NX * bt * 128u;
+                            }
+                        }
+                    }
+                }
+                if (lane == 0) {
+                    uint8_t *st = smem + (size_t)stage * C::STAGE;
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (pages[j] < 0) continue;
+                        const int in_page = (p.page_size > kChunk) ? ((tok0 + j * bt) % p.page_size) : 0;
+#pragma unroll
+                        for (int x = 0; x < C::NX; ++x) {
+                            uint8_t *dk = st + x * C::XTILE + j * bt * 128;
+                            tma_load_4d(dk, &tm_k, &full[stage], x * C::XBOX, h, in_page, pages[j], pol);
+                            tma_load_4d(dk + C::TILE, &tm_v, &full[stage], x * C::XBOX, h, in_page, pages[j], pol);
+                        }
+                    }
+                }
+            }
+        }
+        if (aborted && lane == 0) {
+            // let copies already in flight land before the CTA exits
+            for (int k = max(0, i - C::NS); k < i; ++k)
+                mbar_wait_bounded(&full[k % C::NS], (k / C::NS) & 1, abort_flag, 100000000ull);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int grp = warp / 4, sub = warp % 4;
+    const int r8 = lane >> 2, c4 = lane & 3;
+    const int lrow = lane & 7, lmat = lane >> 3;
+    const int row0 = sub * 16;
+    const int ctid = threadIdx.x;  // 0 .. NCW*32-1
+    const float kscale = FP8 ? p.k_scale[h] : 1.f;
+    const float vscale = FP8 ? p.v_scale[h] : 1.f;
+    const float sl2 = p.scale_log2 * kscale;
+
+    SegWalker wk = make_walker(p.meta, part, p.B);
+    int i = 0;
+    int sb, ss, lc0, lc1;
+    while (wk.next(sb, ss, lc0, lc1)) {
+        const int L = min(max(p.seqlens[sb], 0), max_len);
+        // query fragments (B operand, n = query head r8 of this group)
+        uint32_t qf[C::KS][2];
+        {
+            const size_t qrow = ((size_t)sb * p.H_q + (size_t)h * C::G + r8) * D;
+            if constexpr (!FP8) {
+                const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+                    reinterpret_cast<const __nv_bfloat16 *>(p.q) + qrow);
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    qf[ks][0] = q32[ks * 8 + c4];
+                    qf[ks][1] = q32[ks * 8 + 4 + c4];
+                }
+            } else {
+                const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(p.q) + qrow;
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(qb + ks * 16 + c4 * 4);
+                    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+                    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+                    qf[ks][0] = pack_f16(__low2float(lo), __high2float(lo));
+                    qf[ks][1] = pack_f16(__low2float(hi), __high2float(hi));
+                }
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float acc[C::MT][4];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+        for (int lc = lc0; lc < lc1; ++lc, ++i) {
+            if ((i % C::NGRP) != grp) continue;
+            const int stage = i % C::NS;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(&full[stage], (i / C::NS) & 1, abort_flag, p.wait_limit_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const int nvalid = L - (lc * kChunk + row0);
+            if (nvalid > 0) {
+                const uint32_t ks_base = smem_u32(smem + (size_t)stage * C::STAGE);
+                const uint32_t vs_base = ks_base + C::TILE;
+                // ---- S^T = K Q^T : 16 tokens x 8 heads
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (!FP8) {
+#pragma unroll
+                    for (int ks = 0; ks < C::KS; ++ks) {
+                        const int tok = row0 + lrow + (lmat & 1) * 8;
+                        const int d = ks * 16 + (lmat >> 1) * 8;
+                        const uint32_t addr = ks_base + (d >> 6) * C::XTILE + tok * 128 +
+                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+                        mma_bf16(sacc, a, qf[ks][0], qf[ks][1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const int tok = row0 + lrow + (lmat & 1) * 8;
+                        const int chunk16 = kk * 2 + (lmat >> 1);
+                        const uint32_t addr = ks_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                        uint32_t R[4];
+                        ldsm_x4(addr, R[0], R[1], R[2], R[3]);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint32_t ra = R[hf * 2], rb = R[hf * 2 + 1];
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2((uint16_t)(ra & 0xffff));
+                            a[1] = e4m3x2_to_f16x2((uint16_t)(rb & 0xffff));
+                            a[2] = e4m3x2_to_f16x2((uint16_t)(ra >> 16));
+                            a[3] = e4m3x2_to_f16x2((uint16_t)(rb >> 16));
+                            mma_f16(sacc, a, qf[kk * 2 + hf][0], qf[kk * 2 + hf][1]);
+                        }
+                    }
+                }
+                // ---- online softmax over this warp's 16 tokens (rows r8, r8+8)
+                float s0 = sacc[0] * sl2, s1 = sacc[1] * sl2, s2 = sacc[2] * sl2, s3 = sacc[3] * sl2;
+                if (nvalid < 16) {
+                    if (r8 >= nvalid) s0 = s1 = -INFINITY;
+                    if (r8 + 8 >= nvalid) s2 = s3 = -INFINITY;
+                }
+                const float mn0 = fmaxf(m0, warp_max_xor_4_8_16(fmaxf(s0, s2)));
+                const float mn1 = fmaxf(m1, warp_max_xor_4_8_16(fmaxf(s1, s3)));
+                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+                const float p0 = ex2(s0 - mn0), p1 = ex2(s1 - mn1), p2 = ex2(s2 - mn0), p3 = ex2(s3 - mn1);
+                l0 = l0 * al0 + p0 + p2;
+                l1 = l1 * al1 + p1 + p3;
+                m0 = mn0;
+                m1 = mn1;
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    acc[mt][0] *= al0;
+                    acc[mt][1] *= al1;
+                    acc[mt][2] *= al0;
+                    acc[mt][3] *= al1;
+                }
+                // ---- O^T += V^T P^T
+                uint32_t b0, b1;
+                if constexpr (!FP8) {
+                    b0 = movmatrix_t(pack_bf16(p0, p1));
+                    b1 = movmatrix_t(pack_bf16(p2, p3));
+                } else {
+                    b0 = movmatrix_t(pack_f16(p0, p1));
+                    b1 = movmatrix_t(pack_f16(p2, p3));
+                }
+                const bool tail = nvalid < 16;
+                if constexpr (!FP8) {
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt) {
+                        const int tok = row0 + lrow + (lmat >> 1) * 8;
+                        const int d = mt * 16 + (lmat & 1) * 8;
+                        const uint32_t addr = vs_base + (d >> 6) * C::XTILE + tok * 128 +
+                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+                        if (tail) {
+                            a[0] = keep_tokens(a[0], 2 * c4, nvalid);
+                            a[1] = keep_tokens(a[1], 2 * c4, nvalid);
+                            a[2] = keep_tokens(a[2], 8 + 2 * c4, nvalid);
+                            a[3] = keep_tokens(a[3], 8 + 2 * c4, nvalid);
+                        }
+                        mma_bf16(acc[mt], a, b0, b1);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const int tok = row0 + lrow + (lmat & 1) * 8;
+                        const int chunk16 = kk * 2 + (lmat >> 1);
+                        const uint32_t addr = vs_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                        uint32_t R[4];
+                        ldsm_x4_t(addr, R[0], R[1], R[2], R[3]);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            // bytes of R: [v(t,d), v(t,d+1), v(t+1,d), v(t+1,d+1)] -> token pairs per d
+                            const uint32_t u = prmt(R[hf * 2], 0u, 0x3120u);
+                            const uint32_t w = prmt(R[hf * 2 + 1], 0u, 0x3120u);
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2((uint16_t)(u & 0xffff));
+                            a[1] = e4m3x2_to_f16x2((uint16_t)(u >> 16));
+                            a[2] = e4m3x2_to_f16x2((uint16_t)(w & 0xffff));
+                            a[3] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+                            if (tail) {
+                                a[0] = keep_tokens(a[0], 2 * c4, nvalid);
+                                a[1] = keep_tokens(a[1], 2 * c4, nvalid);
+                                a[2] = keep_tokens(a[2], 8 + 2 * c4, nvalid);
+                                a[3] = keep_tokens(a[3], 8 + 2 * c4, nvalid);
+                            }
+                            mma_f16(acc[kk * 2 + hf], a, b0, b1);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+
+        // ---------------------------------------------------------- merge warps
+        l0 = warp_sum_xor_4_8_16(l0);
+        l1 = warp_sum_xor_4_8_16(l1);
+        if (lane < 4) {
+            sm_m[warp * C::G + 2 * c4] = m0;
+            sm_m[warp * C::G + 2 * c4 + 1] = m1;
+            sm_l[warp * C::G + 2 * c4] = l0;
+            sm_l[warp * C::G + 2 * c4 + 1] = l1;
+        }
+        float *uw = sm_u + (size_t)warp * C::G * C::UPAD;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            // accumulator rows -> head-dim index
+            const int dA = FP8 ? mt * 16 + 2 * r8 : mt * 16 + r8;
+            const int dB = FP8 ? dA + 1 : dA + 8;
+            uw[(2 * c4) * C::UPAD + dA] = acc[mt][0];
+            uw[(2 * c4 + 1) * C::UPAD + dA] = acc[mt][1];
+            uw[(2 * c4) * C::UPAD + dB] = acc[mt][2];
+            uw[(2 * c4 + 1) * C::UPAD + dB] = acc[mt][3];
+        }
+        named_barrier_sync(1, C::NCW * 32);
+        if (ctid < C::G) {
+            const int g = ctid;
+            float M = -INFINITY;
+            for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, sm_m[w * C::G + g]);
+            float Ls = 0.f;
+            for (int w = 0; w < C::NCW; ++w) {
+                const float mw = sm_m[w * C::G + g];
+                const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                sm_w[w * C::G + g] = wt;
+                Ls += wt * sm_l[w * C::G + g];
+            }
+            sm_fin[g] = Ls;
+            sm_fin[C::G + g] = M;
+        }
+        named_barrier_sync(1, C::NCW * 32);
+        const bool direct = p.meta.num_splits[sb] == 1;
+        const int split = p.meta.split_offset[sb] + ss;
+        const bool split_ok = direct || (split >= 0 && split < p.meta.max_splits);
+        for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
+            const int g = idx / D, d = idx % D;
+            float u = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::NCW; ++w) u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
+            const float Ls = sm_fin[g];
+            const float o = (Ls > 0.f) ? (u / Ls) * vscale : 0.f;
+            const size_t hq = (size_t)h * C::G + g;
+            if (direct)
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * p.H_q + hq) * D + d] = __float2bfloat16_rn(o);
+            else if (split_ok)
+                p.meta.o_part[((size_t)split * p.H_q + hq) * D + d] = o;
+        }
+        if (ctid < C::G) {
+            const int g = ctid;
+            const float Ls = sm_fin[g];
+            const float v = (Ls > 0.f) ? (sm_fin[C::G + g] + log2f(Ls)) * kLn2 : -INFINITY;
+            const size_t hq = (size_t)h * C::G + g;
+            if (direct)
+                p.lse[(size_t)sb * p.H_q + hq] = v;
+            else if (split_ok)
+                p.meta.lse_part[(size_t)split * p.H_q + hq] = v;
+        }
+        if (named_barrier_or(1, C::NCW * 32, *abort_flag != 0)) break;
+    }
+}
+
+template <int D, bool FP8>
+static cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
+                              bool pdl) {
+    using C = GqaCfg<D, FP8>;
+    auto kern = gqa_decode_kernel<D, FP8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_parts, p.H_kv);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tk, const CUtensorMap &tv, const GqaParams &p,
+                       cudaStream_t stream, bool pdl) {
+    if (!fp8 && D == 64) return launch_one<64, false>(tk, tv, p, stream, pdl);
+    if (!fp8 && D == 128) return launch_one<128, false>(tk, tv, p, stream, pdl);
+    if (fp8 && D == 128) return launch_one<128, true>(tk, tv, p, stream, pdl);
+    return cudaErrorInvalidValue;
+}
+
+int gqa_box_row_elems(int D, bool fp8) { return fp8 ? 128 : 64; }
+
+}  // namespace da

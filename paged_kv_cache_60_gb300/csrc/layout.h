@@ -1,0 +1,96 @@
+// Host/device shared definitions: sched_meta layout and kernel parameter blocks.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace da {
+
+constexpr int kChunk = 64;                 // tokens per scheduling chunk
+constexpr int32_t kMetaMagic = 0x44414d31;  // "DAM1"
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+// sched_meta header words
+enum MetaHeader : int {
+    kHMagic = 0,
+    kHB = 1,
+    kHHkv = 2,
+    kHG = 3,
+    kHSplits = 4,
+    kHNumParts = 5,
+    kHCpc = 6,
+    kHChunk = 7,
+    kHTotalChunks = 8,
+    kHTotalSplits = 9,
+    kHPer = 10,
+    kHError = 11,
+    kHErrorDetail = 12,
+    kHKvDtype = 13,
+    kHNumSms = 14,
+    kHeaderWords = 16,
+};
+
+struct MetaLayout {
+    size_t header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part, total;
+    int32_t num_parts, max_splits, cpc;
+};
+
+// Device-side view of sched_meta.
+struct MetaView {
+    int32_t *header;
+    const int4 *parts;
+    const int32_t *chunk_offset;
+    const int32_t *split_offset;
+    const int32_t *num_splits;
+    float *lse_part;   // [max_splits][H_q]
+    float *o_part;     // [max_splits][H_q][D_v]
+    int32_t max_splits;
+};
+
+struct SchedParams {
+    const int32_t *seqlens;
+    int32_t *meta;           // header base
+    int32_t *parts;          // int4 records
+    int32_t *chunk_offset;
+    int32_t *split_offset;
+    int32_t *num_splits;
+    int32_t B, H_kv, G, splits, num_parts, cpc, max_len, kv_dtype, num_sms;
+};
+
+struct GqaParams {
+    const void *q;                 // bf16 [B][H_q][D]
+    const int32_t *block_table;    // [B][max_pages]
+    const int32_t *seqlens;        // [B]
+    const float *k_scale;          // [H_kv] (fp8) or null
+    const float *v_scale;
+    MetaView meta;
+    void *out;                     // bf16 [B][H_q][D]
+    float *lse;                    // [B][H_q]
+    int32_t B, H_kv, G, H_q, max_pages, num_pages, page_size, box_tokens, boxes_per_chunk;
+    int32_t splits, num_parts;
+    float scale_log2;              // softmax_scale * log2(e)
+    uint64_t wait_limit_ns;
+};
+
+struct MlaParams {
+    const void *q;                 // bf16 [B][H_q][576]
+    const uint8_t *pool;           // 656-byte tokens
+    const int32_t *block_table;
+    const int32_t *seqlens;
+    MetaView meta;
+    void *out;                     // bf16 [B][H_q][512]
+    float *lse;
+    int32_t B, H_q, max_pages, num_pages, page_size;
+    int32_t splits, num_parts;
+    float scale_log2;
+    uint64_t wait_limit_ns;
+};
+
+struct CombineParams {
+    MetaView meta;
+    void *out;       // bf16 [B][H_q][D_v]
+    float *lse;      // [B][H_q]
+    int32_t B, H_q, D_v, H_kv, G, splits, num_parts;
+};
+
+}  // namespace da

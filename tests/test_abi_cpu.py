@@ -1,0 +1,100 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/decode_attn.h declares, and rejects bad arguments on the host
+with the documented codes before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_60_gb300 as da
+from paged_kv_cache_60_gb300 import build as dabuild
+from oracle.sched_ref import auto_num_parts
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dabuild.build()
+    return da.load_library()
+
+
+def _header_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(decode_attn_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function(lib):
+    names = _header_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(**kw):
+    base = dict(B=4, H_kv=2, G=8, D_qk=128, D_v=128, page_size=16, max_pages_per_seq=10, num_pages=40,
+                kv_dtype=da.KV_BF16, splits=0, num_sms=152)
+    base.update(kw)
+    return da.Desc.make(**base)
+
+
+def test_sched_meta_bytes_and_parts_host_only(lib):
+    d = _desc()
+    n = da.sched_meta_bytes(d)
+    offs = da.meta_offsets(d)
+    assert offs[7] == n and offs[0] == 0 and offs[1] == 64
+    assert all(o % 16 == 0 for o in offs)
+    assert offs[5] % 256 == 0 and offs[6] % 256 == 0
+    assert da.num_parts(d) == auto_num_parts(152, 2, 1) == 76
+    parts = 76
+    max_splits = parts + 4
+    assert offs[6] - offs[5] >= max_splits * 16 * 4
+    assert n - offs[6] >= max_splits * 16 * 128 * 4
+    d2 = _desc(splits=8)
+    assert da.num_parts(d2) == 32
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("B", 0, -2), ("H_kv", 0, -2), ("page_size", 12, -3), ("G", 4, -3), ("D_qk", 96, -3),
+    ("splits", -1, -5), ("kv_dtype", 7, -3), ("max_pages_per_seq", 0, -2),
+])
+def test_bad_desc_codes(lib, field, value, code):
+    d = _desc(**{field: value})
+    n = ctypes.c_size_t(0)
+    assert lib.decode_attn_sched_meta_bytes(ctypes.byref(d), ctypes.byref(n)) == code
+
+
+def test_fp8_needs_d128_and_mla_shape(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.decode_attn_sched_meta_bytes(ctypes.byref(_desc(kv_dtype=da.KV_FP8, D_qk=64, D_v=64)),
+                                            ctypes.byref(n)) == -3
+    assert lib.decode_attn_sched_meta_bytes(ctypes.byref(_desc(kv_dtype=da.KV_FP8)), ctypes.byref(n)) == 0
+
+
+def test_fwd_rejects_null_and_misaligned_before_launch(lib):
+    d = _desc()
+    n = da.sched_meta_bytes(d)
+    P = ctypes.c_void_p
+    good = P(0x10000)
+    bad = P(0x10008)
+    args = lambda q=good, meta=good: (ctypes.byref(d), q, good, good, None, None, good, good, meta, n,  # noqa: E731
+                                      good, good, None)
+    assert lib.decode_attn_fwd(*args(q=None)) == -1
+    assert lib.decode_attn_fwd(*args(q=bad)) == -4
+    assert lib.decode_attn_fwd(ctypes.byref(d), good, good, good, None, None, good, good, good, n - 16,
+                               good, good, None) == -6
+    dq = _desc(kv_dtype=da.KV_FP8)
+    nq = da.sched_meta_bytes(dq)
+    assert lib.decode_attn_fwd(ctypes.byref(dq), good, good, good, None, None, good, good, good, nq,
+                               good, good, None) == -8
+
+
+def test_strerror_is_total(lib):
+    for c in range(-10, 2):
+        assert isinstance(da.strerror(c), str) and da.strerror(c)
