@@ -260,7 +260,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
     const MetaView mv = meta_view(sched_meta, L);
     const int H_q = desc->H_kv * desc->G;
 
-    if (opts && opts->main_begin && cudaEventRecord(opts->main_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
+    const cudaEvent_t ev_begin = opts ? opts->main_begin : nullptr;
     if (!mla) {
         const bool fp8 = desc->kv_dtype == DA_KV_FP8_PER_TENSOR;
         const int es = fp8 ? 1 : 2;
@@ -291,6 +291,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
         p.wait_limit_ns = kWaitLimitNs;
+        if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_gqa(desc->D_qk, fp8, tk, tv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     } else {
         MlaParams p;
@@ -310,6 +311,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
         p.wait_limit_ns = kWaitLimitNs;
+        if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     }
     if (opts && opts->main_end && cudaEventRecord(opts->main_end, stream) != cudaSuccess) return DA_ERR_CUDA;
