@@ -109,9 +109,12 @@ int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
  * header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part,
  * total size. Header (16 int32): magic, B, H_kv, G, splits, num_parts, cpc,
  * chunk (64), total_chunks, total_splits, per, error word, error detail,
- * kv_dtype, num_sms, reserved. parts: num_parts records {b0, s0, c0, c1}
- * (first request, its split index there, global chunk interval [c0, c1)).
- * chunk_offset, split_offset: int32 [B+1] prefix sums; num_splits: int32 [B].
+ * kv_dtype, num_sms, reserved. parts: num_parts records of 8 int32
+ * {b0, s0, c0, c1, co0, L0, so0, ns0}: first request, its split index there,
+ * global chunk interval [c0, c1), then chunk_offset[b0], min(L_b0,
+ * max_pages_per_seq*page_size), split_offset[b0], num_splits[b0] (all 0 when
+ * b0 = -1, a part with no work). chunk_offset, split_offset: int32 [B+1]
+ * prefix sums; num_splits: int32 [B].
  */
 int decode_attn_meta_offsets(const da_desc *desc, size_t offs[8]);
 

@@ -97,7 +97,7 @@ int make_layout(const da_desc *d, MetaLayout *L) {
     L->header = off;
     off += kHeaderWords * 4;
     L->parts = off;
-    off += round_up((size_t)num_parts * 16, 16);
+    off += round_up((size_t)num_parts * sizeof(PartRec), 16);
     L->chunk_offset = off;
     off += round_up((size_t)(d->B + 1) * 4, 16);
     L->split_offset = off;

@@ -20,25 +20,27 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int DV>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
     pdl_wait();
-    {
-        const int32_t *hd = p.meta.header;
-        if (!(hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv && hd[kHG] == p.G &&
-              hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts))
-            return;  // the split-KV kernel has flagged the mismatch
-    }
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.y * 4 + warp;
-    if (hq >= p.H_q) return;
+    // independent loads first, then the checks
+    const int32_t *hd = p.meta.header;
     const int ns = p.meta.num_splits[b];
-    if (ns == 1) return;  // written directly by the split-KV kernel
     const int so = p.meta.split_offset[b];
+    if (!(hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv && hd[kHG] == p.G &&
+          hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts))
+        return;  // the split-KV kernel has flagged the mismatch
+    if (hq >= p.H_q) return;
+    if (ns == 1) return;  // written directly by the split-KV kernel
     if (ns < 0 || so < 0 || so + ns > p.meta.max_splits) return;
     constexpr int PER_LANE = DV / 32;
     static_assert(DV % 64 == 0, "DV must be a multiple of 64");
     const float *lp = p.meta.lse_part + (size_t)so * p.H_q + hq;
+    // lane s holds split s's lse (splits beyond 32 are folded in a loop)
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[(size_t)s * p.H_q]);
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, lp[(size_t)s * p.H_q]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)b * p.H_q + hq) * DV;
     float acc[PER_LANE];
 #pragma unroll
@@ -46,23 +48,33 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     float lse_v = -INFINITY;
     if (M != -INFINITY) {
         float Z = 0.f;
-        for (int s = 0; s < ns; ++s) Z += ex2((lp[(size_t)s * p.H_q] - M) * kLog2e);
-        lse_v = M + logf(Z);
-        for (int s = 0; s < ns; ++s) {
-            const float w = ex2((lp[(size_t)s * p.H_q] - lse_v) * kLog2e);
-            const float *src = p.meta.o_part + (((size_t)(so + s)) * p.H_q + hq) * DV;
-            if constexpr (PER_LANE == 2) {
-                const float2 v = reinterpret_cast<const float2 *>(src)[lane];
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-            } else {
+        for (int s = lane; s < ns; s += 32) Z += ex2((lp[(size_t)s * p.H_q] - M) * kLog2e);
+        // fixed-order tree sum over lanes
 #pragma unroll
-                for (int k4 = 0; k4 < PER_LANE / 4; ++k4) {
-                    const float4 v = reinterpret_cast<const float4 *>(src)[k4 * 32 + lane];
-                    acc[k4 * 4 + 0] += w * v.x;
-                    acc[k4 * 4 + 1] += w * v.y;
-                    acc[k4 * 4 + 2] += w * v.z;
-                    acc[k4 * 4 + 3] += w * v.w;
+        for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
+        lse_v = M + logf(Z);
+        for (int s0 = 0; s0 < ns; s0 += 32) {
+            const int cnt = min(32, ns - s0);
+            const float w_l = (lane < cnt) ? ex2((lp[(size_t)(s0 + lane) * p.H_q] - lse_v) * kLog2e) : 0.f;
+            const float *src0 = p.meta.o_part + (((size_t)(so + s0)) * p.H_q + hq) * DV;
+            const size_t sstride = (size_t)p.H_q * DV;
+#pragma unroll 4
+            for (int s = 0; s < cnt; ++s) {
+                const float w = __shfl_sync(0xffffffffu, w_l, s);
+                const float *src = src0 + s * sstride;
+                if constexpr (PER_LANE == 2) {
+                    const float2 v = reinterpret_cast<const float2 *>(src)[lane];
+                    acc[0] += w * v.x;
+                    acc[1] += w * v.y;
+                } else {
+#pragma unroll
+                    for (int k4 = 0; k4 < PER_LANE / 4; ++k4) {
+                        const float4 v = reinterpret_cast<const float4 *>(src)[k4 * 32 + lane];
+                        acc[k4 * 4 + 0] += w * v.x;
+                        acc[k4 * 4 + 1] += w * v.y;
+                        acc[k4 * 4 + 2] += w * v.z;
+                        acc[k4 * 4 + 3] += w * v.w;
+                    }
                 }
             }
         }

@@ -29,8 +29,9 @@
 //    two values per cvt; the per-tensor scales are folded into the score scale
 //    (k_scale) and into the output (v_scale) (same page, section
 //    "Hopper 路径上 V 不做显式反量化").
-//  * every consumer warp owns 16 tokens of a chunk and keeps its own
-//    (m, l, O) state; at the end of a segment the warps' states are merged
+//  * every consumer warp takes whole chunks (round robin) as four independent
+//    16-token tiles, so its MMA chains and shuffle reductions interleave, and
+//    keeps its own (m, l, O) state; at the end of a segment the warps' states are merged
 //    through shared memory in a fixed order, and the segment's result is
 //    written either as the final bf16 output (request has one split) or as a
 //    float32 partial plus its lse for the combine kernel.
@@ -54,9 +55,8 @@ struct GqaCfg {
     static constexpr int TILE = kChunk * ROW;
     static constexpr int XTILE = kChunk * 128;  // one x-box column of a tile
     static constexpr int STAGE = 2 * TILE;
-    static constexpr int NCW = 8;            // consumer warps
-    static constexpr int NGRP = NCW / 4;     // consumer groups (alternate chunks)
-    static constexpr int NS = FP8 ? 8 : (D == 128 ? 5 : 4);
+    static constexpr int NCW = 8;            // consumer warps, one chunk each (round robin)
+    static constexpr int NS = FP8 ? 12 : (D == 128 ? 6 : 5);
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int MT = D / 16;
     static constexpr int KS = D / 16;
@@ -74,31 +74,61 @@ struct GqaCfg {
     static_assert(!FP8 || NX == 1, "fp8 path expects one 128-byte box per row");
 };
 
-// Walks the (request, split, local chunk range) segments of one part.
+// One (request, split, local chunk range) piece of a part, with the request's
+// clamped length, split base and split count.
+struct Seg {
+    int b, s, lc0, lc1, L, so, ns;
+};
+
+// Walks the segments of one part. The first segment comes entirely from the
+// part record (no dependent loads); later ones read the per-request arrays.
 struct SegWalker {
-    const int32_t *chunk_offset;
-    int B, b, s, c, c1;
-    bool pending_empty;
-    __device__ bool next(int &sb, int &ss, int &lc0, int &lc1) {
+    const int32_t *chunk_offset, *split_offset, *num_splits, *seqlens;
+    int B, max_len, b, s, c, c1;
+    int co0, L0, so0, ns0;
+    bool first, pending_empty;
+    __device__ bool next(Seg &g) {
         if (pending_empty) {
             pending_empty = false;
-            sb = b;
-            ss = s;
-            lc0 = lc1 = c - chunk_offset[b];
+            g.b = b;
+            g.s = s;
+            g.lc0 = g.lc1 = c - co0;
+            g.L = L0;
+            g.so = so0;
+            g.ns = ns0;
             c = c1;
             return true;
         }
         if (b < 0 || c >= c1) return false;
-        while (b < B && chunk_offset[b + 1] <= c) {
-            ++b;
-            s = 0;
+        int cb, ce;
+        if (first) {
+            cb = co0;
+            ce = chunk_offset[b + 1];
+            if (ce <= c) return false;  // inconsistent record
+        } else {
+            while (b < B && chunk_offset[b + 1] <= c) {
+                ++b;
+                s = 0;
+            }
+            if (b >= B) return false;
+            cb = chunk_offset[b];
+            ce = chunk_offset[b + 1];
         }
-        if (b >= B) return false;
-        const int end = min(c1, chunk_offset[b + 1]);
-        sb = b;
-        ss = s;
-        lc0 = c - chunk_offset[b];
-        lc1 = end - chunk_offset[b];
+        const int end = min(c1, ce);
+        g.b = b;
+        g.s = s;
+        g.lc0 = c - cb;
+        g.lc1 = end - cb;
+        if (first) {
+            g.L = L0;
+            g.so = so0;
+            g.ns = ns0;
+        } else {
+            g.L = min(max(seqlens[b], 0), max_len);
+            g.so = split_offset[b];
+            g.ns = num_splits[b];
+        }
+        first = false;
         c = end;
         ++b;
         s = 0;
@@ -106,17 +136,26 @@ struct SegWalker {
     }
 };
 
-__device__ __forceinline__ SegWalker make_walker(const MetaView &mv, int part, int B) {
-    int4 r = mv.parts[part];
-    if (r.x >= B || r.z > r.w) r.x = -1;  // not a record this desc can produce
+__device__ __forceinline__ SegWalker make_walker(const MetaView &mv, const int4 r0, const int4 r1, int B,
+                                                 const int32_t *seqlens, int max_len) {
     SegWalker w;
     w.chunk_offset = mv.chunk_offset;
+    w.split_offset = mv.split_offset;
+    w.num_splits = mv.num_splits;
+    w.seqlens = seqlens;
     w.B = B;
-    w.b = r.x;
-    w.s = r.y;
-    w.c = r.z;
-    w.c1 = r.w;
-    w.pending_empty = (r.x >= 0) && (r.z == r.w);
+    w.max_len = max_len;
+    const bool valid = r0.x >= 0 && r0.x < B && r0.z <= r0.w;
+    w.b = valid ? r0.x : -1;
+    w.s = r0.y;
+    w.c = r0.z;
+    w.c1 = r0.w;
+    w.co0 = r1.x;
+    w.L0 = r1.y;
+    w.so0 = r1.z;
+    w.ns0 = r1.w;
+    w.first = true;
+    w.pending_empty = valid && (r0.z == r0.w);
     return w;
 }
 
@@ -148,7 +187,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 4);
+            mbar_init(&empty[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -162,6 +201,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
     pdl_wait();
     pdl_launch_dependents();
 
+    // the part record and the header are independent loads: issue both, then check
+    const int4 rec0 = p.meta.parts[2 * part];
+    const int4 rec1 = p.meta.parts[2 * part + 1];
     {
         const int32_t *hd = p.meta.header;
         const bool ok = hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv &&
@@ -173,17 +215,18 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         }
     }
     const int max_len = p.max_pages * p.page_size;
+    // parts beyond the header's count are never read: the check above ties gridDim.x to it
 
     if (warp == C::NCW) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = policy_evict_first();
-        SegWalker wk = make_walker(p.meta, part, p.B);
+        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
         int i = 0;
         bool aborted = false;
-        int sb, ss, lc0, lc1;
-        while (!aborted && wk.next(sb, ss, lc0, lc1)) {
+        Seg sg;
+        while (!aborted && wk.next(sg)) {
+            const int sb = sg.b, lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
             if (lc0 == lc1) continue;
-            const int L = min(max(p.seqlens[sb], 0), max_len);
             const int nb = p.boxes_per_chunk, bt = p.box_tokens;
             const int total_boxes = (lc1 - lc0) * nb;
             const int tok_base = lc0 * kChunk;
@@ -261,20 +304,18 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
     }
 
     // ---------------------------------------------------------------- consumers
-    const int grp = warp / 4, sub = warp % 4;
     const int r8 = lane >> 2, c4 = lane & 3;
     const int lrow = lane & 7, lmat = lane >> 3;
-    const int row0 = sub * 16;
     const int ctid = threadIdx.x;  // 0 .. NCW*32-1
     const float kscale = FP8 ? p.k_scale[h] : 1.f;
     const float vscale = FP8 ? p.v_scale[h] : 1.f;
     const float sl2 = p.scale_log2 * kscale;
 
-    SegWalker wk = make_walker(p.meta, part, p.B);
+    SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
     int i = 0;
-    int sb, ss, lc0, lc1;
-    while (wk.next(sb, ss, lc0, lc1)) {
-        const int L = min(max(p.seqlens[sb], 0), max_len);
+    Seg sg;
+    while (wk.next(sg)) {
+        const int sb = sg.b, ss = sg.s, lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
         // query fragments (B operand, n = query head r8 of this group)
         uint32_t qf[C::KS][2];
         {
@@ -305,7 +346,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         for (int mt = 0; mt < C::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
         for (int lc = lc0; lc < lc1; ++lc, ++i) {
-            if ((i % C::NGRP) != grp) continue;
+            if ((i % C::NCW) != warp) continue;  // one warp per chunk, round robin
             const int stage = i % C::NS;
             int ok = 1;
             if (lane == 0) ok = mbar_wait_bounded(&full[stage], (i / C::NS) & 1, abort_flag, p.wait_limit_ns);
@@ -317,116 +358,150 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 }
                 break;
             }
-            const int nvalid = L - (lc * kChunk + row0);
-            if (nvalid > 0) {
-                const uint32_t ks_base = smem_u32(smem + (size_t)stage * C::STAGE);
-                const uint32_t vs_base = ks_base + C::TILE;
-                // ---- S^T = K Q^T : 16 tokens x 8 heads
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (!FP8) {
+            const int nvalid = L - lc * kChunk;  // >= 1: valid tokens of this chunk
+            const uint32_t ks_base = smem_u32(smem + (size_t)stage * C::STAGE);
+            const uint32_t vs_base = ks_base + C::TILE;
+            // ---- S^T = K Q^T for four independent 16-token tiles
+            float sacc[4][4];
 #pragma unroll
-                    for (int ks = 0; ks < C::KS; ++ks) {
-                        const int tok = row0 + lrow + (lmat & 1) * 8;
-                        const int d = ks * 16 + (lmat >> 1) * 8;
-                        const uint32_t addr = ks_base + (d >> 6) * C::XTILE + tok * 128 +
-                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
-                        uint32_t a[4];
-                        ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-                        mma_bf16(sacc, a, qf[ks][0], qf[ks][1]);
-                    }
-                } else {
+            for (int t = 0; t < 4; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+            if constexpr (!FP8) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk) {
-                        const int tok = row0 + lrow + (lmat & 1) * 8;
-                        const int chunk16 = kk * 2 + (lmat >> 1);
-                        const uint32_t addr = ks_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
-                        uint32_t R[4];
-                        ldsm_x4(addr, R[0], R[1], R[2], R[3]);
+                for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const uint32_t ra = R[hf * 2], rb = R[hf * 2 + 1];
+                    for (int t = 0; t < 4; ++t) {
+                        if (16 * t < nvalid) {
+                            const int tok = 16 * t + lrow + (lmat & 1) * 8;
+                            const int d = ks * 16 + (lmat >> 1) * 8;
+                            const uint32_t addr = ks_base + (d >> 6) * C::XTILE + tok * 128 +
+                                                  ((((d & 63) >> 3) ^ (tok & 7)) << 4);
                             uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2((uint16_t)(ra & 0xffff));
-                            a[1] = e4m3x2_to_f16x2((uint16_t)(rb & 0xffff));
-                            a[2] = e4m3x2_to_f16x2((uint16_t)(ra >> 16));
-                            a[3] = e4m3x2_to_f16x2((uint16_t)(rb >> 16));
-                            mma_f16(sacc, a, qf[kk * 2 + hf][0], qf[kk * 2 + hf][1]);
+                            ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+                            mma_bf16(sacc[t], a, qf[ks][0], qf[ks][1]);
                         }
                     }
                 }
-                // ---- online softmax over this warp's 16 tokens (rows r8, r8+8)
-                float s0 = sacc[0] * sl2, s1 = sacc[1] * sl2, s2 = sacc[2] * sl2, s3 = sacc[3] * sl2;
-                if (nvalid < 16) {
-                    if (r8 >= nvalid) s0 = s1 = -INFINITY;
-                    if (r8 + 8 >= nvalid) s2 = s3 = -INFINITY;
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        if (16 * t < nvalid) {
+                            const int tok = 16 * t + lrow + (lmat & 1) * 8;
+                            const int chunk16 = kk * 2 + (lmat >> 1);
+                            const uint32_t addr = ks_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                            uint32_t R[4];
+                            ldsm_x4(addr, R[0], R[1], R[2], R[3]);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const uint32_t ra = R[hf * 2], rb = R[hf * 2 + 1];
+                                uint32_t a[4];
+                                a[0] = e4m3x2_to_f16x2((uint16_t)(ra & 0xffff));
+                                a[1] = e4m3x2_to_f16x2((uint16_t)(rb & 0xffff));
+                                a[2] = e4m3x2_to_f16x2((uint16_t)(ra >> 16));
+                                a[3] = e4m3x2_to_f16x2((uint16_t)(rb >> 16));
+                                mma_f16(sacc[t], a, qf[kk * 2 + hf][0], qf[kk * 2 + hf][1]);
+                            }
+                        }
+                    }
                 }
-                const float mn0 = fmaxf(m0, warp_max_xor_4_8_16(fmaxf(s0, s2)));
-                const float mn1 = fmaxf(m1, warp_max_xor_4_8_16(fmaxf(s1, s3)));
-                const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-                const float p0 = ex2(s0 - mn0), p1 = ex2(s1 - mn1), p2 = ex2(s2 - mn0), p3 = ex2(s3 - mn1);
-                l0 = l0 * al0 + p0 + p2;
-                l1 = l1 * al1 + p1 + p3;
-                m0 = mn0;
-                m1 = mn1;
+            }
+            // ---- online softmax over the chunk's 64 tokens (rows 16t + r8, 16t + r8 + 8)
+            float sv[4][4];
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const bool va = 16 * t + r8 < nvalid, vb = 16 * t + r8 + 8 < nvalid;
+                sv[t][0] = va ? sacc[t][0] * sl2 : -INFINITY;
+                sv[t][1] = va ? sacc[t][1] * sl2 : -INFINITY;
+                sv[t][2] = vb ? sacc[t][2] * sl2 : -INFINITY;
+                sv[t][3] = vb ? sacc[t][3] * sl2 : -INFINITY;
+                mx0 = fmaxf(mx0, fmaxf(sv[t][0], sv[t][2]));
+                mx1 = fmaxf(mx1, fmaxf(sv[t][1], sv[t][3]));
+            }
+            const float mn0 = fmaxf(m0, warp_max_xor_4_8_16(mx0));
+            const float mn1 = fmaxf(m1, warp_max_xor_4_8_16(mx1));
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            float ps0 = 0.f, ps1 = 0.f;
+            uint32_t pb[4][2];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float p0 = ex2(sv[t][0] - mn0), p1 = ex2(sv[t][1] - mn1);
+                const float p2 = ex2(sv[t][2] - mn0), p3 = ex2(sv[t][3] - mn1);
+                ps0 += p0 + p2;
+                ps1 += p1 + p3;
+                if constexpr (!FP8) {
+                    pb[t][0] = movmatrix_t(pack_bf16(p0, p1));
+                    pb[t][1] = movmatrix_t(pack_bf16(p2, p3));
+                } else {
+                    pb[t][0] = movmatrix_t(pack_f16(p0, p1));
+                    pb[t][1] = movmatrix_t(pack_f16(p2, p3));
+                }
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                acc[mt][0] *= al0;
+                acc[mt][1] *= al1;
+                acc[mt][2] *= al0;
+                acc[mt][3] *= al1;
+            }
+            // ---- O^T += V^T P^T
+            const bool tail = nvalid < kChunk;
+            if constexpr (!FP8) {
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) {
-                    acc[mt][0] *= al0;
-                    acc[mt][1] *= al1;
-                    acc[mt][2] *= al0;
-                    acc[mt][3] *= al1;
-                }
-                // ---- O^T += V^T P^T
-                uint32_t b0, b1;
-                if constexpr (!FP8) {
-                    b0 = movmatrix_t(pack_bf16(p0, p1));
-                    b1 = movmatrix_t(pack_bf16(p2, p3));
-                } else {
-                    b0 = movmatrix_t(pack_f16(p0, p1));
-                    b1 = movmatrix_t(pack_f16(p2, p3));
-                }
-                const bool tail = nvalid < 16;
-                if constexpr (!FP8) {
 #pragma unroll
-                    for (int mt = 0; mt < C::MT; ++mt) {
-                        const int tok = row0 + lrow + (lmat >> 1) * 8;
-                        const int d = mt * 16 + (lmat & 1) * 8;
-                        const uint32_t addr = vs_base + (d >> 6) * C::XTILE + tok * 128 +
-                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
-                        uint32_t a[4];
-                        ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
-                        if (tail) {
-                            a[0] = keep_tokens(a[0], 2 * c4, nvalid);
-                            a[1] = keep_tokens(a[1], 2 * c4, nvalid);
-                            a[2] = keep_tokens(a[2], 8 + 2 * c4, nvalid);
-                            a[3] = keep_tokens(a[3], 8 + 2 * c4, nvalid);
-                        }
-                        mma_bf16(acc[mt], a, b0, b1);
-                    }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk) {
-                        const int tok = row0 + lrow + (lmat & 1) * 8;
-                        const int chunk16 = kk * 2 + (lmat >> 1);
-                        const uint32_t addr = vs_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
-                        uint32_t R[4];
-                        ldsm_x4_t(addr, R[0], R[1], R[2], R[3]);
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            // bytes of R: [v(t,d), v(t,d+1), v(t+1,d), v(t+1,d+1)] -> token pairs per d
-                            const uint32_t u = prmt(R[hf * 2], 0u, 0x3120u);
-                            const uint32_t w = prmt(R[hf * 2 + 1], 0u, 0x3120u);
+                    for (int t = 0; t < 4; ++t) {
+                        if (16 * t < nvalid) {
+                            const int tok = 16 * t + lrow + (lmat >> 1) * 8;
+                            const int d = mt * 16 + (lmat & 1) * 8;
+                            const uint32_t addr = vs_base + (d >> 6) * C::XTILE + tok * 128 +
+                                                  ((((d & 63) >> 3) ^ (tok & 7)) << 4);
                             uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2((uint16_t)(u & 0xffff));
-                            a[1] = e4m3x2_to_f16x2((uint16_t)(u >> 16));
-                            a[2] = e4m3x2_to_f16x2((uint16_t)(w & 0xffff));
-                            a[3] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+                            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
                             if (tail) {
-                                a[0] = keep_tokens(a[0], 2 * c4, nvalid);
-                                a[1] = keep_tokens(a[1], 2 * c4, nvalid);
-                                a[2] = keep_tokens(a[2], 8 + 2 * c4, nvalid);
-                                a[3] = keep_tokens(a[3], 8 + 2 * c4, nvalid);
+                                a[0] = keep_tokens(a[0], 16 * t + 2 * c4, nvalid);
+                                a[1] = keep_tokens(a[1], 16 * t + 2 * c4, nvalid);
+                                a[2] = keep_tokens(a[2], 16 * t + 8 + 2 * c4, nvalid);
+                                a[3] = keep_tokens(a[3], 16 * t + 8 + 2 * c4, nvalid);
                             }
-                            mma_f16(acc[kk * 2 + hf], a, b0, b1);
+                            mma_bf16(acc[mt], a, pb[t][0], pb[t][1]);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        if (16 * t < nvalid) {
+                            const int tok = 16 * t + lrow + (lmat & 1) * 8;
+                            const int chunk16 = kk * 2 + (lmat >> 1);
+                            const uint32_t addr = vs_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                            uint32_t R[4];
+                            ldsm_x4_t(addr, R[0], R[1], R[2], R[3]);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                // bytes of R: [v(t,d), v(t,d+1), v(t+1,d), v(t+1,d+1)] -> token pairs per d
+                                const uint32_t u = prmt(R[hf * 2], 0u, 0x3120u);
+                                const uint32_t w = prmt(R[hf * 2 + 1], 0u, 0x3120u);
+                                uint32_t a[4];
+                                a[0] = e4m3x2_to_f16x2((uint16_t)(u & 0xffff));
+                                a[1] = e4m3x2_to_f16x2((uint16_t)(u >> 16));
+                                a[2] = e4m3x2_to_f16x2((uint16_t)(w & 0xffff));
+                                a[3] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+                                if (tail) {
+                                    a[0] = keep_tokens(a[0], 16 * t + 2 * c4, nvalid);
+                                    a[1] = keep_tokens(a[1], 16 * t + 2 * c4, nvalid);
+                                    a[2] = keep_tokens(a[2], 16 * t + 8 + 2 * c4, nvalid);
+                                    a[3] = keep_tokens(a[3], 16 * t + 8 + 2 * c4, nvalid);
+                                }
+                                mma_f16(acc[kk * 2 + hf], a, pb[t][0], pb[t][1]);
+                            }
                         }
                     }
                 }
@@ -471,8 +546,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
             sm_fin[C::G + g] = M;
         }
         named_barrier_sync(1, C::NCW * 32);
-        const bool direct = p.meta.num_splits[sb] == 1;
-        const int split = p.meta.split_offset[sb] + ss;
+        const bool direct = sg.ns == 1;
+        const int split = sg.so + ss;
         const bool split_ok = direct || (split >= 0 && split < p.meta.max_splits);
         for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
             const int g = idx / D, d = idx % D;

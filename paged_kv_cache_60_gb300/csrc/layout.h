@@ -30,6 +30,15 @@ enum MetaHeader : int {
     kHeaderWords = 16,
 };
 
+// One part record (32 bytes): the part's first request b0, that request's
+// split index s0 there, the global chunk interval [c0, c1), and -- so that the
+// split-KV kernel needs no further dependent load for the first segment --
+// chunk_offset[b0], min(L_b0, max_len), split_offset[b0], num_splits[b0].
+struct PartRec {
+    int32_t b0, s0, c0, c1, co0, L0, so0, ns0;
+};
+constexpr int kPartRecInts = 8;
+
 struct MetaLayout {
     size_t header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part, total;
     int32_t num_parts, max_splits, cpc;
@@ -38,7 +47,7 @@ struct MetaLayout {
 // Device-side view of sched_meta.
 struct MetaView {
     int32_t *header;
-    const int4 *parts;
+    const int4 *parts;            // PartRec as two int4 per part
     const int32_t *chunk_offset;
     const int32_t *split_offset;
     const int32_t *num_splits;
@@ -50,7 +59,7 @@ struct MetaView {
 struct SchedParams {
     const int32_t *seqlens;
     int32_t *meta;           // header base
-    int32_t *parts;          // int4 records
+    int32_t *parts;          // PartRec records
     int32_t *chunk_offset;
     int32_t *split_offset;
     int32_t *num_splits;

@@ -44,14 +44,25 @@ __device__ __forceinline__ int block_incl_scan(int v, int *warp_sums, int &total
     return v;
 }
 
+constexpr int kSmemReq = 4096;  // requests whose prefix sums stay in shared memory
+
 __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant__ SchedParams p) {
     __shared__ int warp_sums[32];
     __shared__ int s_err;
+    __shared__ int s_co[kSmemReq + 1];  // chunk_offset
+    __shared__ int s_so[kSmemReq + 1];  // split_offset
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x;
-    if (tid == 0) s_err = 0;
+    const bool in_smem = p.B <= kSmemReq;
+    if (tid == 0) {
+        s_err = 0;
+        s_co[0] = 0;
+        s_so[0] = 0;
+    }
     __syncthreads();
+    // chunk_offset[b] from shared memory when it fits, else from global memory
+    auto co = [&](int b) -> int { return in_smem ? s_co[b] : p.chunk_offset[b]; };
 
     // pass 1: chunks per request and their prefix sum
     int carry = 0;
@@ -72,7 +83,10 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
         }
         int tile_total;
         const int incl = block_incl_scan(n, warp_sums, tile_total);
-        if (b < p.B) p.chunk_offset[b + 1] = carry + incl;
+        if (b < p.B) {
+            p.chunk_offset[b + 1] = carry + incl;
+            if (in_smem) s_co[b + 1] = carry + incl;
+        }
         carry += tile_total;
     }
     if (tid == 0) p.chunk_offset[0] = 0;
@@ -86,52 +100,65 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
         const int b = base + tid;
         int ns = 0;
         if (b < p.B) {
-            const int co = p.chunk_offset[b], cn = p.chunk_offset[b + 1];
+            const int c0 = co(b), cn = co(b + 1);
             if (p.splits > 0)
                 ns = p.splits;
-            else if (cn > co)
-                ns = (cn - 1) / per - co / per + 1;
+            else if (cn > c0)
+                ns = (cn - 1) / per - c0 / per + 1;
             p.num_splits[b] = ns;
         }
         int tile_total;
         const int incl = block_incl_scan(ns, warp_sums, tile_total);
-        if (b < p.B) p.split_offset[b + 1] = carry + incl;
+        if (b < p.B) {
+            p.split_offset[b + 1] = carry + incl;
+            if (in_smem) s_so[b + 1] = carry + incl;
+        }
         carry += tile_total;
     }
     if (tid == 0) p.split_offset[0] = 0;
     const int total_splits = carry;
     __syncthreads();
+    auto so = [&](int b) -> int { return in_smem ? s_so[b] : p.split_offset[b]; };
 
     // pass 3: one record per part
     for (int q = tid; q < p.num_parts; q += blockDim.x) {
-        int4 rec;
+        int b0, s0, c0, c1;
         if (p.splits > 0) {
-            const int b = q / p.splits, s = q % p.splits;
-            const int co = p.chunk_offset[b];
-            const int n = p.chunk_offset[b + 1] - co;
+            b0 = q / p.splits;
+            s0 = q % p.splits;
+            const int cb = co(b0);
+            const int n = co(b0 + 1) - cb;
             const int per_b = (n + p.splits - 1) / p.splits;
-            const int lo = min(s * per_b, n), hi = min((s + 1) * per_b, n);
-            rec = make_int4(b, s, co + lo, co + hi);
+            c0 = cb + min(s0 * per_b, n);
+            c1 = cb + min((s0 + 1) * per_b, n);
         } else {
-            const int c0 = (int)min((long long)q * per, (long long)total);
-            const int c1 = min(c0 + per, total);
+            c0 = (int)min((long long)q * per, (long long)total);
+            c1 = min(c0 + per, total);
             if (c0 >= total) {
-                rec = make_int4(-1, 0, total, total);
+                b0 = -1;
+                s0 = 0;
             } else {
                 // first i in [0, B] with chunk_offset[i] > c0, minus one
                 int lo = 0, hi = p.B;
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
-                    if (p.chunk_offset[mid] > c0)
+                    if (co(mid) > c0)
                         hi = mid;
                     else
                         lo = mid + 1;
                 }
-                const int b = lo - 1;
-                rec = make_int4(b, q - p.chunk_offset[b] / per, c0, c1);
+                b0 = lo - 1;
+                s0 = q - co(b0) / per;
             }
         }
-        reinterpret_cast<int4 *>(p.parts)[q] = rec;
+        int4 *rec = reinterpret_cast<int4 *>(p.parts) + 2 * q;
+        rec[0] = make_int4(b0, s0, c0, c1);
+        if (b0 >= 0) {
+            const int L0 = min(max(p.seqlens[b0], 0), p.max_len);
+            rec[1] = make_int4(co(b0), L0, so(b0), p.splits > 0 ? p.splits : so(b0 + 1) - so(b0));
+        } else {
+            rec[1] = make_int4(0, 0, 0, 0);
+        }
     }
     __syncthreads();
     if (tid == 0) {

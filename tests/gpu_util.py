@@ -64,10 +64,23 @@ def read_meta(meta, desc):
         return m[offs[a]:offs[a] + 4 * n].view(torch.int32).tolist()
     header = i32(0, 16)
     nparts = header[5]
-    parts = m[offs[1]:offs[1] + 16 * nparts].view(torch.int32).view(nparts, 4).tolist()
+    recs = m[offs[1]:offs[1] + 32 * nparts].view(torch.int32).view(nparts, 8).tolist()
     B = desc.B
-    return dict(header=header, parts=[tuple(p) for p in parts], chunk_offset=i32(2, B + 1),
+    return dict(header=header, parts=[tuple(p[:4]) for p in recs], part_extra=[tuple(p[4:]) for p in recs],
+                chunk_offset=i32(2, B + 1),
                 split_offset=i32(3, B + 1), num_splits=i32(4, B))
+
+
+def expected_part_extra(ref, seqlens, max_len):
+    """The four cached per-part fields, derived from the oracle's arrays."""
+    out = []
+    for (b0, s0, c0, c1) in ref.parts:
+        if b0 < 0:
+            out.append((0, 0, 0, 0))
+        else:
+            out.append((ref.chunk_offset[b0], min(max(seqlens[b0], 0), max_len), ref.split_offset[b0],
+                        ref.num_splits[b0]))
+    return out
 
 
 def max_err(out, lse, ref_out, ref_lse, heads=None, G=None):

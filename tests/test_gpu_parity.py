@@ -13,8 +13,8 @@ from oracle.sched_ref import sched_ref
 from workloads import CONFIGS, WorkloadSpec, make_workload, spec_by_name, KV_BF16, KV_FP8
 from workloads.gen import repermute_pages
 
-from gpu_util import (LSE_TOL, OUT_TOL, DeviceWorkload, device_sms, ensure_built, make_desc, max_err,
-                      read_meta, run)
+from gpu_util import (LSE_TOL, OUT_TOL, DeviceWorkload, device_sms, ensure_built, expected_part_extra,
+                      make_desc, max_err, read_meta, run)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +61,7 @@ def test_sched_meta_bit_exact(seqlens, splits, H_kv):
     assert h[0] == 0x44414d31 and h[1] == B and h[5] == ref.num_parts
     assert h[8] == ref.total_chunks and h[9] == ref.total_splits and h[10] == ref.per and h[11] == 0
     assert got["parts"] == ref.parts
+    assert got["part_extra"] == expected_part_extra(ref, seqlens, maxp * P)
     assert got["chunk_offset"] == ref.chunk_offset
     assert got["split_offset"] == ref.split_offset
     assert got["num_splits"] == ref.num_splits
@@ -80,6 +81,7 @@ def test_sched_meta_large_batch_bit_exact():
         ref = sched_ref(seqlens, 1, splits, device_sms())
         assert got["parts"] == ref.parts and got["split_offset"] == ref.split_offset
         assert got["chunk_offset"] == ref.chunk_offset and got["num_splits"] == ref.num_splits
+        assert got["part_extra"] == expected_part_extra(ref, seqlens, maxp * P)
 
 
 # ------------------------------------------------------------------ attention, small cases
