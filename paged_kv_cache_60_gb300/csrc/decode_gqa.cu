@@ -55,8 +55,14 @@ struct GqaCfg {
     static constexpr int TILE = kChunk * ROW;
     static constexpr int XTILE = kChunk * 128;  // one x-box column of a tile
     static constexpr int STAGE = 2 * TILE;
-    static constexpr int NCW = 8;            // consumer warps, one chunk each (round robin)
+    // consumer warps (one chunk each, round robin) and ring stages. NS is a
+    // multiple of NCW so that stage s is always consumed by warp s % NCW: a
+    // warp then waits on the phases of a stage one after the other, and never
+    // on a phase two ahead of the barrier's current one (whose parity would
+    // alias an already completed phase).
+    static constexpr int NCW = D == 64 ? 5 : 6;
     static constexpr int NS = FP8 ? 12 : (D == 128 ? 6 : 5);
+    static_assert(NS % NCW == 0, "stage ownership must be fixed per warp");
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int MT = D / 16;
     static constexpr int KS = D / 16;
