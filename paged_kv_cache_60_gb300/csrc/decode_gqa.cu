@@ -165,12 +165,6 @@ __device__ __forceinline__ SegWalker make_walker(const MetaView &mv, const int4 
     return w;
 }
 
-__device__ __forceinline__ uint32_t keep_tokens(uint32_t x, int t_even, int nvalid) {
-    const uint32_t lo = (t_even < nvalid) ? 0x0000ffffu : 0u;
-    const uint32_t hi = (t_even + 1 < nvalid) ? 0xffff0000u : 0u;
-    return x & (lo | hi);
-}
-
 template <int D, bool FP8>
 __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_BLOCKS)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -246,9 +240,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
             for (int lc = lc0; lc < lc1; ++lc, ++i) {
                 const int stage = i % C::NS;
                 const uint32_t par = ((i / C::NS) & 1) ^ 1;
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait_bounded(&empty[stage], par, abort_flag, p.wait_limit_ns);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                const bool ok = mbar_wait_warp(&empty[stage], par, abort_flag, p.wait_limit_ns);
                 if (!ok) {
                     if (lane == 0) {
                         atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
@@ -354,10 +346,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         for (int lc = lc0; lc < lc1; ++lc, ++i) {
             if ((i % C::NCW) != warp) continue;  // one warp per chunk, round robin
             const int stage = i % C::NS;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait_bounded(&full[stage], (i / C::NS) & 1, abort_flag, p.wait_limit_ns);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
+            if (!mbar_wait_warp(&full[stage], (i / C::NS) & 1, abort_flag, p.wait_limit_ns)) {
                 if (lane == 0) {
                     atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
                     *abort_flag = 1;
@@ -365,8 +354,22 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 break;
             }
             const int nvalid = L - lc * kChunk;  // >= 1: valid tokens of this chunk
-            const uint32_t ks_base = smem_u32(smem + (size_t)stage * C::STAGE);
+            uint8_t *stage_ptr = smem + (size_t)stage * C::STAGE;
+            const uint32_t ks_base = smem_u32(stage_ptr);
             const uint32_t vs_base = ks_base + C::TILE;
+            const bool tail = nvalid < kChunk;
+            if (tail) {
+                // rows past the sequence end hold stale or poisoned bytes: zero them
+                // in V so that 0-weight tokens contribute exactly 0 (S is masked below)
+                uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + C::TILE);
+                const int nrow = kChunk - nvalid;
+                for (int e = lane; e < nrow * C::NX * 8; e += 32) {
+                    const int x = e / (nrow * 8), rem = e % (nrow * 8);
+                    const int row = nvalid + rem / 8, c16 = rem % 8;
+                    vrow[(x * C::XTILE + row * 128) / 16 + c16] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
             // ---- S^T = K Q^T for four independent 16-token tiles
             float sacc[4][4];
 #pragma unroll
@@ -376,15 +379,13 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        if (16 * t < nvalid) {
-                            const int tok = 16 * t + lrow + (lmat & 1) * 8;
-                            const int d = ks * 16 + (lmat >> 1) * 8;
-                            const uint32_t addr = ks_base + (d >> 6) * C::XTILE + tok * 128 +
-                                                  ((((d & 63) >> 3) ^ (tok & 7)) << 4);
-                            uint32_t a[4];
-                            ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-                            mma_bf16(sacc[t], a, qf[ks][0], qf[ks][1]);
-                        }
+                        const int tok = 16 * t + lrow + (lmat & 1) * 8;
+                        const int d = ks * 16 + (lmat >> 1) * 8;
+                        const uint32_t addr = ks_base + (d >> 6) * C::XTILE + tok * 128 +
+                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+                        mma_bf16(sacc[t], a, qf[ks][0], qf[ks][1]);
                     }
                 }
             } else {
@@ -392,22 +393,20 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int kk = 0; kk < D / 32; ++kk) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        if (16 * t < nvalid) {
-                            const int tok = 16 * t + lrow + (lmat & 1) * 8;
-                            const int chunk16 = kk * 2 + (lmat >> 1);
-                            const uint32_t addr = ks_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
-                            uint32_t R[4];
-                            ldsm_x4(addr, R[0], R[1], R[2], R[3]);
+                        const int tok = 16 * t + lrow + (lmat & 1) * 8;
+                        const int chunk16 = kk * 2 + (lmat >> 1);
+                        const uint32_t addr = ks_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                        uint32_t R[4];
+                        ldsm_x4(addr, R[0], R[1], R[2], R[3]);
 #pragma unroll
-                            for (int hf = 0; hf < 2; ++hf) {
-                                const uint32_t ra = R[hf * 2], rb = R[hf * 2 + 1];
-                                uint32_t a[4];
-                                a[0] = e4m3x2_to_f16x2((uint16_t)(ra & 0xffff));
-                                a[1] = e4m3x2_to_f16x2((uint16_t)(rb & 0xffff));
-                                a[2] = e4m3x2_to_f16x2((uint16_t)(ra >> 16));
-                                a[3] = e4m3x2_to_f16x2((uint16_t)(rb >> 16));
-                                mma_f16(sacc[t], a, qf[kk * 2 + hf][0], qf[kk * 2 + hf][1]);
-                            }
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint32_t ra = R[hf * 2], rb = R[hf * 2 + 1];
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2((uint16_t)(ra & 0xffff));
+                            a[1] = e4m3x2_to_f16x2((uint16_t)(rb & 0xffff));
+                            a[2] = e4m3x2_to_f16x2((uint16_t)(ra >> 16));
+                            a[3] = e4m3x2_to_f16x2((uint16_t)(rb >> 16));
+                            mma_f16(sacc[t], a, qf[kk * 2 + hf][0], qf[kk * 2 + hf][1]);
                         }
                     }
                 }
@@ -456,27 +455,18 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 acc[mt][3] *= al1;
             }
             // ---- O^T += V^T P^T
-            const bool tail = nvalid < kChunk;
             if constexpr (!FP8) {
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        if (16 * t < nvalid) {
-                            const int tok = 16 * t + lrow + (lmat >> 1) * 8;
-                            const int d = mt * 16 + (lmat & 1) * 8;
-                            const uint32_t addr = vs_base + (d >> 6) * C::XTILE + tok * 128 +
-                                                  ((((d & 63) >> 3) ^ (tok & 7)) << 4);
-                            uint32_t a[4];
-                            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
-                            if (tail) {
-                                a[0] = keep_tokens(a[0], 16 * t + 2 * c4, nvalid);
-                                a[1] = keep_tokens(a[1], 16 * t + 2 * c4, nvalid);
-                                a[2] = keep_tokens(a[2], 16 * t + 8 + 2 * c4, nvalid);
-                                a[3] = keep_tokens(a[3], 16 * t + 8 + 2 * c4, nvalid);
-                            }
-                            mma_bf16(acc[mt], a, pb[t][0], pb[t][1]);
-                        }
+                        const int tok = 16 * t + lrow + (lmat >> 1) * 8;
+                        const int d = mt * 16 + (lmat & 1) * 8;
+                        const uint32_t addr = vs_base + (d >> 6) * C::XTILE + tok * 128 +
+                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+                        mma_bf16(acc[mt], a, pb[t][0], pb[t][1]);
                     }
                 }
             } else {
@@ -484,34 +474,27 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int kk = 0; kk < D / 32; ++kk) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        if (16 * t < nvalid) {
-                            const int tok = 16 * t + lrow + (lmat & 1) * 8;
-                            const int chunk16 = kk * 2 + (lmat >> 1);
-                            const uint32_t addr = vs_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
-                            uint32_t R[4];
-                            ldsm_x4_t(addr, R[0], R[1], R[2], R[3]);
+                        const int tok = 16 * t + lrow + (lmat & 1) * 8;
+                        const int chunk16 = kk * 2 + (lmat >> 1);
+                        const uint32_t addr = vs_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                        uint32_t R[4];
+                        ldsm_x4_t(addr, R[0], R[1], R[2], R[3]);
 #pragma unroll
-                            for (int hf = 0; hf < 2; ++hf) {
-                                // bytes of R: [v(t,d), v(t,d+1), v(t+1,d), v(t+1,d+1)] -> token pairs per d
-                                const uint32_t u = prmt(R[hf * 2], 0u, 0x3120u);
-                                const uint32_t w = prmt(R[hf * 2 + 1], 0u, 0x3120u);
-                                uint32_t a[4];
-                                a[0] = e4m3x2_to_f16x2((uint16_t)(u & 0xffff));
-                                a[1] = e4m3x2_to_f16x2((uint16_t)(u >> 16));
-                                a[2] = e4m3x2_to_f16x2((uint16_t)(w & 0xffff));
-                                a[3] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
-                                if (tail) {
-                                    a[0] = keep_tokens(a[0], 16 * t + 2 * c4, nvalid);
-                                    a[1] = keep_tokens(a[1], 16 * t + 2 * c4, nvalid);
-                                    a[2] = keep_tokens(a[2], 16 * t + 8 + 2 * c4, nvalid);
-                                    a[3] = keep_tokens(a[3], 16 * t + 8 + 2 * c4, nvalid);
-                                }
-                                mma_f16(acc[kk * 2 + hf], a, pb[t][0], pb[t][1]);
-                            }
+                        for (int hf = 0; hf < 2; ++hf) {
+                            // bytes of R: [v(t,d), v(t,d+1), v(t+1,d), v(t+1,d+1)] -> token pairs per d
+                            const uint32_t u = prmt(R[hf * 2], 0u, 0x3120u);
+                            const uint32_t w = prmt(R[hf * 2 + 1], 0u, 0x3120u);
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2((uint16_t)(u & 0xffff));
+                            a[1] = e4m3x2_to_f16x2((uint16_t)(u >> 16));
+                            a[2] = e4m3x2_to_f16x2((uint16_t)(w & 0xffff));
+                            a[3] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+                            mma_f16(acc[kk * 2 + hf], a, pb[t][0], pb[t][1]);
                         }
                     }
                 }
             }
+            if (tail) fence_proxy_async_smem();  // generic writes above, TMA writes next
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
