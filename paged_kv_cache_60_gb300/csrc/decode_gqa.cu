@@ -60,8 +60,8 @@ struct GqaCfg {
     // warp then waits on the phases of a stage one after the other, and never
     // on a phase two ahead of the barrier's current one (whose parity would
     // alias an already completed phase).
-    static constexpr int NCW = D == 64 ? 5 : 6;
-    static constexpr int NS = FP8 ? 12 : (D == 128 ? 6 : 5);
+    static constexpr int NCW = FP8 ? 10 : (D == 64 ? 5 : 6);
+    static constexpr int NS = FP8 ? 10 : (D == 128 ? 6 : 5);
     static_assert(NS % NCW == 0, "stage ownership must be fixed per warp");
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int MT = D / 16;
