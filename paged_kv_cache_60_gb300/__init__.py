@@ -135,7 +135,12 @@ def fwd(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seql
     if use_pdl and main_begin is None and main_end is None:
         _check(lib.decode_attn_fwd(*args, _stream(stream)))
     else:
-        ev = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)  # noqa: E731
+        def ev(e):
+            if e is None:
+                return None
+            if not e.cuda_event:     # torch creates events lazily, at their first record
+                e.record()
+            return ctypes.c_void_p(e.cuda_event)
         opts = LaunchOpts(1 if use_pdl else 0, ev(main_begin), ev(main_end))
         _check(lib.decode_attn_fwd_ex(*args, ctypes.byref(opts), _stream(stream)))
 

@@ -12,8 +12,7 @@
 
 namespace da {
 cudaError_t launch_sched_meta(const SchedParams &p, cudaStream_t stream, bool pdl);
-cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tk, const CUtensorMap &tv, const GqaParams &p,
-                       cudaStream_t stream, bool pdl);
+cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const GqaParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl);
 int mla_ctas_per_part();
@@ -148,20 +147,25 @@ EncodeTiledFn get_encode_tiled() {
     return fn;
 }
 
-// Pool [num_pages][P][H_kv][D] as a 4-D map; box = 128 bytes x 1 head x box_tok tokens x 1 page.
-int make_pool_map(CUtensorMap *m, const void *pool, const da_desc *d, int elem_bytes, int box_tok) {
+// Both pools as one 5-D map over 8-byte elements:
+//   dim 0: 16 elements = 128 bytes          dim 1: NX halves of a head row (stride 128 B)
+//   dim 2: KV head (stride = row)           dim 3: global token = page*P + slot (stride row*H_kv)
+//   dim 4: pool, K or V (stride = distance between the two pools)
+// and a box {16, NX, 1, box_tok, 2}: one copy brings one page's K and V rows of
+// one head. base is the lower of the two pools.
+int make_kv_map(CUtensorMap *m, const void *base, uint64_t pool_dist, const da_desc *d, int elem_bytes,
+                int box_tok) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return DA_ERR_CUDA;
-    const int D = d->D_qk;
-    const cuuint64_t row = (cuuint64_t)D * elem_bytes;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)d->H_kv, (cuuint64_t)d->page_size, (cuuint64_t)d->num_pages};
-    cuuint64_t strides[3] = {row, row * d->H_kv, row * d->H_kv * d->page_size};
-    cuuint32_t box[4] = {(cuuint32_t)(128 / elem_bytes), 1, (cuuint32_t)box_tok, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUtensorMapDataType dt =
-        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    CUresult r = enc(m, dt, 4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t row = (cuuint64_t)d->D_qk * elem_bytes;  // bytes of one token's head
+    const cuuint64_t nx = row / 128;
+    cuuint64_t dims[5] = {128 / kTmaElemBytes, nx, (cuuint64_t)d->H_kv,
+                          (cuuint64_t)d->page_size * (cuuint64_t)d->num_pages, 2};
+    cuuint64_t strides[4] = {128, row, row * d->H_kv, pool_dist};
+    cuuint32_t box[5] = {128 / kTmaElemBytes, (cuuint32_t)nx, 1, (cuuint32_t)box_tok, 2};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 5, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
@@ -266,9 +270,14 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         const int es = fp8 ? 1 : 2;
         const int P = desc->page_size;
         const int box_tok = P < kChunk ? P : kChunk;
-        CUtensorMap tk, tv;
-        if ((rc = make_pool_map(&tk, k_pool, desc, es, box_tok))) return rc;
-        if ((rc = make_pool_map(&tv, v_pool, desc, es, box_tok))) return rc;
+        // the two pools must be distinct, non-overlapping buffers
+        const uint64_t pool_bytes = (uint64_t)desc->num_pages * P * desc->H_kv * desc->D_qk * es;
+        const uintptr_t ka = reinterpret_cast<uintptr_t>(k_pool), va = reinterpret_cast<uintptr_t>(v_pool);
+        const uint64_t dist = ka > va ? (uint64_t)(ka - va) : (uint64_t)(va - ka);
+        if (dist < pool_bytes || dist >= (1ull << 40)) return DA_ERR_UNSUPPORTED;
+        if ((int64_t)P * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+        CUtensorMap tkv;
+        if ((rc = make_kv_map(&tkv, ka < va ? k_pool : v_pool, dist, desc, es, box_tok))) return rc;
         GqaParams p;
         p.q = q;
         p.block_table = block_table;
@@ -287,12 +296,14 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.page_size = P;
         p.box_tokens = box_tok;
         p.boxes_per_chunk = kChunk / box_tok;
+        p.log2_box_tokens = box_tok == 8 ? 3 : box_tok == 16 ? 4 : box_tok == 32 ? 5 : 6;
+        p.kv_swap = va < ka ? 1 : 0;
         p.splits = desc->splits;
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
         p.wait_limit_ns = kWaitLimitNs;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
-        if (launch_gqa(desc->D_qk, fp8, tk, tv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
+        if (launch_gqa(desc->D_qk, fp8, tkv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     } else {
         MlaParams p;
         p.q = q;

@@ -50,11 +50,9 @@ struct GqaCfg {
     static constexpr int G = 8;
     static constexpr int ES = FP8 ? 1 : 2;
     static constexpr int ROW = D * ES;       // bytes of one token's head
-    static constexpr int NX = ROW / 128;     // 128-byte TMA boxes per row
-    static constexpr int XBOX = 128 / ES;    // elements per box row
+    static constexpr int NX = ROW / 128;     // 128-byte halves of a row
     static constexpr int TILE = kChunk * ROW;
-    static constexpr int XTILE = kChunk * 128;  // one x-box column of a tile
-    static constexpr int STAGE = 2 * TILE;
+    static constexpr int STAGE = 2 * TILE;   // K and V of one chunk
     // consumer warps (one chunk each, round robin) and ring stages. NS is a
     // multiple of NCW so that stage s is always consumed by warp s % NCW: a
     // warp then waits on the phases of a stage one after the other, and never
@@ -167,8 +165,7 @@ __device__ __forceinline__ SegWalker make_walker(const MetaView &mv, const int4 
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_BLOCKS)
-    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ GqaParams p) {
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ GqaParams p) {
     using C = GqaCfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -186,7 +183,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], p.boxes_per_chunk);  // one arrival per producer lane
             mbar_init(&empty[i], 1);
         }
         *abort_flag = 0;
@@ -194,8 +191,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         fence_proxy_async_smem();
     }
     if (warp == C::NCW && lane == 0) {
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_kv);
     }
     __syncthreads();
     pdl_wait();
@@ -219,81 +215,62 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
 
     if (warp == C::NCW) {
         // ------------------------------------------------------------ producer
+        // Lane j < boxes_per_chunk owns box j of every chunk: one TMA per page
+        // brings that page's K and V rows of head h (both pools, both 128-byte
+        // halves of a row, through one 5-D tensor map). Each lane keeps the
+        // page ids of its next four chunks in registers, loaded four chunks
+        // ahead, arrives on the chunk's full barrier with its own byte count
+        // and issues its own copy -- no shuffles, no load latency in the loop.
+        const int nb = p.boxes_per_chunk, bt = p.box_tokens, P = p.page_size;
+        if (lane >= nb) return;
         const uint64_t pol = policy_evict_first();
+        const uint32_t box_bytes = 2u * bt * C::NX * 128u;
         SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
         int i = 0;
         bool aborted = false;
         Seg sg;
         while (!aborted && wk.next(sg)) {
-            const int sb = sg.b, lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
+            const int lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
             if (lc0 == lc1) continue;
-            const int nb = p.boxes_per_chunk, bt = p.box_tokens;
-            const int total_boxes = (lc1 - lc0) * nb;
-            const int tok_base = lc0 * kChunk;
-            const int32_t *bt_row = p.block_table + (size_t)sb * p.max_pages;
-            auto page_of = [&](int gb) -> int {
-                const int tok = tok_base + gb * bt;
-                if (gb >= total_boxes || tok >= L) return -1;
-                return bt_row[tok / p.page_size];
+            const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
+            // page id of this lane's box in chunk lc, or -2 when the box lies past the sequence
+            auto id_of = [&](int lc) -> int {
+                const int tok = lc * kChunk + lane * bt;
+                return (lc < lc1 && tok < L) ? bt_row[tok / P] : -2;
             };
-            int cur = page_of(lane), nxt = page_of(32 + lane), cur_base = 0;
-            for (int lc = lc0; lc < lc1; ++lc, ++i) {
-                const int stage = i % C::NS;
-                const uint32_t par = ((i / C::NS) & 1) ^ 1;
-                const bool ok = mbar_wait_warp(&empty[stage], par, abort_flag, p.wait_limit_ns);
-                if (!ok) {
-                    if (lane == 0) {
+            int ring[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ring[k] = id_of(lc0 + k);
+            for (int lc = lc0; lc < lc1 && !aborted; lc += 4) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (lc + k >= lc1) break;
+                    int pg = ring[k];
+                    ring[k] = id_of(lc + k + 4);
+                    const int stage = i % C::NS;
+                    if (!mbar_wait_bounded(&empty[stage], ((i / C::NS) & 1) ^ 1, abort_flag, p.wait_limit_ns)) {
                         atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
                         *abort_flag = 1;
+                        aborted = true;
+                        break;
                     }
-                    aborted = true;
-                    break;
-                }
-                const int tok0 = lc * kChunk;
-                int pages[8];
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    pages[j] = -1;
-                    if (j < nb) {
-                        const int gb = (lc - lc0) * nb + j;
-                        if (gb - cur_base >= 32) {
-                            cur = nxt;
-                            cur_base += 32;
-                            nxt = page_of(cur_base + 32 + lane);
-                        }
-                        const int pg = __shfl_sync(0xffffffffu, cur, gb - cur_base);
-                        if (tok0 + j * bt < L) {
-                            if (pg < 0 || pg >= p.num_pages) {
-                                if (lane == 0) {
-                                    atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
-                                    p.meta.header[kHErrorDetail] = pg;
-                                }
-                            } else {
-                                pages[j] = pg;
-                                bytes += 2u * C::NX * bt * 128u;
-                            }
-                        }
+                    if (pg != -2 && (pg < 0 || pg >= p.num_pages)) {
+                        atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
+                        p.meta.header[kHErrorDetail] = pg;
+                        pg = -2;  // skipped: its rows keep stale bytes
                     }
-                }
-                if (lane == 0) {
-                    uint8_t *st = smem + (size_t)stage * C::STAGE;
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (pages[j] < 0) continue;
-                        const int in_page = (p.page_size > kChunk) ? ((tok0 + j * bt) % p.page_size) : 0;
-#pragma unroll
-                        for (int x = 0; x < C::NX; ++x) {
-                            uint8_t *dk = st + x * C::XTILE + j * bt * 128;
-                            tma_load_4d(dk, &tm_k, &full[stage], x * C::XBOX, h, in_page, pages[j], pol);
-                            tma_load_4d(dk + C::TILE, &tm_v, &full[stage], x * C::XBOX, h, in_page, pages[j], pol);
-                        }
+                    mbar_arrive_expect_tx(&full[stage], pg == -2 ? 0u : box_bytes);
+                    if (pg != -2) {
+                        const int tok = (lc + k) * kChunk + lane * bt;
+                        const int in_page = (P > kChunk) ? (tok % P) : 0;
+                        uint8_t *st = smem + (size_t)stage * C::STAGE + lane * box_bytes;
+                        tma_load_5d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, 0, pol);
                     }
+                    ++i;
                 }
             }
         }
-        if (aborted && lane == 0) {
+        if (aborted) {
             // let copies already in flight land before the CTA exits
             for (int k = max(0, i - C::NS); k < i; ++k)
                 mbar_wait_bounded(&full[k % C::NS], (k / C::NS) & 1, abort_flag, 100000000ull);
@@ -308,6 +285,29 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
     const float kscale = FP8 ? p.k_scale[h] : 1.f;
     const float vscale = FP8 ? p.v_scale[h] : 1.f;
     const float sl2 = p.scale_log2 * kscale;
+    // Stage layout: box j (tokens [j*bt, (j+1)*bt)) at j*box_bytes holds
+    // [first pool][bt tokens][NX halves][128 B], then the same for the second
+    // pool; p.kv_swap tells which pool comes first. With bt >= 8 every box and
+    // half starts on a 1024-byte boundary, so the 128-byte swizzle key of
+    // token t, half x is (t*NX + x) & 7.
+    const int bt = p.box_tokens, lbt = p.log2_box_tokens;
+    const uint32_t half_bytes = (uint32_t)bt * C::NX * 128u;
+    const uint32_t k_half = p.kv_swap ? half_bytes : 0u, v_half = p.kv_swap ? 0u : half_bytes;
+    auto row_of = [&](int tok) -> uint32_t {
+        return (uint32_t)((tok >> lbt) * 2 * bt + (tok & (bt - 1))) * (C::NX * 128u);
+    };
+    // tokens this lane addresses in ldmatrix: tile t, 8-row half sel
+    uint32_t rk[4], rv[4];
+    int keyk[4], keyv[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int tk = 16 * t + lrow + (lmat & 1) * 8;                      // K rows (QK), V rows (fp8 PV)
+        const int tv = FP8 ? tk : 16 * t + lrow + (lmat >> 1) * 8;          // V rows (bf16 PV)
+        rk[t] = row_of(tk) + k_half;
+        rv[t] = row_of(tv) + v_half;
+        keyk[t] = (tk * C::NX) & 7;
+        keyv[t] = (tv * C::NX) & 7;
+    }
 
     SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
     int i = 0;
@@ -355,18 +355,16 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
             }
             const int nvalid = L - lc * kChunk;  // >= 1: valid tokens of this chunk
             uint8_t *stage_ptr = smem + (size_t)stage * C::STAGE;
-            const uint32_t ks_base = smem_u32(stage_ptr);
-            const uint32_t vs_base = ks_base + C::TILE;
+            const uint32_t s_base = smem_u32(stage_ptr);
             const bool tail = nvalid < kChunk;
             if (tail) {
                 // rows past the sequence end hold stale or poisoned bytes: zero them
                 // in V so that 0-weight tokens contribute exactly 0 (S is masked below)
-                uint4 *vrow = reinterpret_cast<uint4 *>(stage_ptr + C::TILE);
                 const int nrow = kChunk - nvalid;
                 for (int e = lane; e < nrow * C::NX * 8; e += 32) {
-                    const int x = e / (nrow * 8), rem = e % (nrow * 8);
-                    const int row = nvalid + rem / 8, c16 = rem % 8;
-                    vrow[(x * C::XTILE + row * 128) / 16 + c16] = make_uint4(0u, 0u, 0u, 0u);
+                    const int tok = nvalid + e / (C::NX * 8), c16 = e % (C::NX * 8);
+                    uint4 *vr = reinterpret_cast<uint4 *>(stage_ptr + row_of(tok) + v_half);
+                    vr[c16] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 __syncwarp();
             }
@@ -379,10 +377,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int tok = 16 * t + lrow + (lmat & 1) * 8;
                         const int d = ks * 16 + (lmat >> 1) * 8;
-                        const uint32_t addr = ks_base + (d >> 6) * C::XTILE + tok * 128 +
-                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
+                        const int x = d >> 6;
+                        const uint32_t addr = s_base + rk[t] + x * 128 + ((((d & 63) >> 3) ^ (keyk[t] + x)) << 4);
                         uint32_t a[4];
                         ldsm_x4(addr, a[0], a[1], a[2], a[3]);
                         mma_bf16(sacc[t], a, qf[ks][0], qf[ks][1]);
@@ -393,9 +390,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int kk = 0; kk < D / 32; ++kk) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int tok = 16 * t + lrow + (lmat & 1) * 8;
                         const int chunk16 = kk * 2 + (lmat >> 1);
-                        const uint32_t addr = ks_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                        const uint32_t addr = s_base + rk[t] + ((chunk16 ^ keyk[t]) << 4);
                         uint32_t R[4];
                         ldsm_x4(addr, R[0], R[1], R[2], R[3]);
 #pragma unroll
@@ -460,10 +456,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int tok = 16 * t + lrow + (lmat >> 1) * 8;
                         const int d = mt * 16 + (lmat & 1) * 8;
-                        const uint32_t addr = vs_base + (d >> 6) * C::XTILE + tok * 128 +
-                                              ((((d & 63) >> 3) ^ (tok & 7)) << 4);
+                        const int x = d >> 6;
+                        const uint32_t addr = s_base + rv[t] + x * 128 + ((((d & 63) >> 3) ^ (keyv[t] + x)) << 4);
                         uint32_t a[4];
                         ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
                         mma_bf16(acc[mt], a, pb[t][0], pb[t][1]);
@@ -474,9 +469,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 for (int kk = 0; kk < D / 32; ++kk) {
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int tok = 16 * t + lrow + (lmat & 1) * 8;
                         const int chunk16 = kk * 2 + (lmat >> 1);
-                        const uint32_t addr = vs_base + tok * 128 + ((chunk16 ^ (tok & 7)) << 4);
+                        const uint32_t addr = s_base + rv[t] + ((chunk16 ^ keyv[t]) << 4);
                         uint32_t R[4];
                         ldsm_x4_t(addr, R[0], R[1], R[2], R[3]);
 #pragma unroll
@@ -566,8 +560,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
 }
 
 template <int D, bool FP8>
-static cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
-                              bool pdl) {
+static cudaError_t launch_one(const CUtensorMap &tkv, const GqaParams &p, cudaStream_t stream, bool pdl) {
     using C = GqaCfg<D, FP8>;
     auto kern = gqa_decode_kernel<D, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -582,17 +575,15 @@ static cudaError_t launch_one(const CUtensorMap &tk, const CUtensorMap &tv, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, kern, tkv, p);
 }
 
-cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tk, const CUtensorMap &tv, const GqaParams &p,
-                       cudaStream_t stream, bool pdl) {
-    if (!fp8 && D == 64) return launch_one<64, false>(tk, tv, p, stream, pdl);
-    if (!fp8 && D == 128) return launch_one<128, false>(tk, tv, p, stream, pdl);
-    if (fp8 && D == 128) return launch_one<128, true>(tk, tv, p, stream, pdl);
+cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const GqaParams &p, cudaStream_t stream, bool pdl) {
+    if (!fp8 && D == 64) return launch_one<64, false>(tkv, p, stream, pdl);
+    if (!fp8 && D == 128) return launch_one<128, false>(tkv, p, stream, pdl);
+    if (fp8 && D == 128) return launch_one<128, true>(tkv, p, stream, pdl);
     return cudaErrorInvalidValue;
 }
 
-int gqa_box_row_elems(int D, bool fp8) { return fp8 ? 128 : 64; }
 
 }  // namespace da

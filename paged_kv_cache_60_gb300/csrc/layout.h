@@ -7,6 +7,7 @@
 namespace da {
 
 constexpr int kChunk = 64;                 // tokens per scheduling chunk
+constexpr int kTmaElemBytes = 8;           // element size the pool tensor maps are described with
 constexpr int32_t kMetaMagic = 0x44414d31;  // "DAM1"
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
@@ -76,6 +77,8 @@ struct GqaParams {
     void *out;                     // bf16 [B][H_q][D]
     float *lse;                    // [B][H_q]
     int32_t B, H_kv, G, H_q, max_pages, num_pages, page_size, box_tokens, boxes_per_chunk;
+    int32_t log2_box_tokens;       // box_tokens is 8, 16, 32 or 64
+    int32_t kv_swap;               // 1: the V pool lies below the K pool (its rows come first in a box)
     int32_t splits, num_parts;
     float scale_log2;              // softmax_scale * log2(e)
     uint64_t wait_limit_ns;
