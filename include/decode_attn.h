@@ -176,6 +176,34 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
  */
 int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStream_t stream);
 
+/* Size of the library's fixed device scratch buffer (16 MiB). */
+#define DA_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * decode_attn_sched_meta + decode_attn_fwd in one call that allocates
+ * nothing and needs no caller-provided scratch. (No counterpart on the source
+ * pages: it exists for deployment.) It is meant for callers that cannot
+ * allocate device memory or hand the library a buffer -- a server that plans
+ * all device memory up front and may not call cudaMalloc later, a plug-in that
+ * cannot reach its host's allocator, a real-time path that must not risk an
+ * allocation.
+ *
+ * The scheduling metadata and the split-KV partials live in a static device
+ * array of DA_STATIC_SCRATCH_BYTES that the library owns; every GPU that loads
+ * the library keeps it until the process exits. Problems whose
+ * decode_attn_sched_meta_bytes exceeds that size are rejected with
+ * DA_ERR_META_SIZE. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current): make that first
+ * call before any stream capture. Every call reuses the same array and leaves
+ * its contents behind; the scheduling kernel rewrites all it reads, so nothing
+ * needs clearing, but calls whose work overlaps on the GPU race on the array.
+ * Arguments, layouts and errors are those of decode_attn_fwd; device errors
+ * land in the array's error word and are not readable from outside.
+ */
+int decode_attn_fwd_static_scratch(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                                   const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                   const int32_t *cache_seqlens, void *out, float *lse, cudaStream_t stream);
+
 /* Static description of a return code (never NULL). */
 const char *decode_attn_strerror(int code);
 

@@ -145,6 +145,22 @@ def fwd(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seql
         _check(lib.decode_attn_fwd_ex(*args, ctypes.byref(opts), _stream(stream)))
 
 
+def fwd_static_scratch(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seqlens, out, lse,
+                       stream=None):
+    """sched_meta + fwd without any caller scratch, for callers that cannot
+    allocate device memory; see decode_attn_fwd_static_scratch in the header
+    (fixed 16 MiB library buffer, first call per device before any capture,
+    overlapping calls race)."""
+    lib = load_library()
+    f = lib.decode_attn_fwd_static_scratch
+    if f.restype is not ctypes.c_int:
+        P = ctypes.c_void_p
+        f.argtypes = [ctypes.POINTER(Desc), P, P, P, P, P, P, P, P, P, P]
+        f.restype = ctypes.c_int
+    _check(f(ctypes.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+             _ptr(block_table), _ptr(cache_seqlens), _ptr(out), _ptr(lse), _stream(stream)))
+
+
 def get_error(meta, stream=None) -> int:
     e = ctypes.c_int32(0)
     _check(load_library().decode_attn_get_error(_ptr(meta), ctypes.byref(e), _stream(stream)))
@@ -152,4 +168,4 @@ def get_error(meta, stream=None) -> int:
 
 
 __all__ = ["Desc", "LaunchOpts", "DecodeAttnError", "load_library", "strerror", "sched_meta_bytes",
-           "meta_offsets", "num_parts", "sched_meta", "fwd", "get_error", "KV_BF16", "KV_FP8", "KV_MLA656"]
+           "meta_offsets", "num_parts", "sched_meta", "fwd", "fwd_static_scratch", "get_error", "KV_BF16", "KV_FP8", "KV_MLA656"]
