@@ -48,9 +48,7 @@ extern "C" {
 
 /* KV cache formats. */
 typedef enum {
-    /* k_pool, v_pool: bf16 [num_pages][page_size][H_kv][D], D = D_qk = D_v.
-     * For this and the next format the two pools must be distinct,
-     * non-overlapping buffers less than 2^40 bytes apart. */
+    /* k_pool, v_pool: bf16 [num_pages][page_size][H_kv][D], D = D_qk = D_v. */
     DA_KV_BF16 = 0,
     /* k_pool, v_pool: float8 e4m3 bytes [num_pages][page_size][H_kv][D];
      * element value = e4m3 * k_scale[h] (resp. v_scale[h]), one fp32 scale per

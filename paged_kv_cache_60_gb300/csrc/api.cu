@@ -12,7 +12,8 @@
 
 namespace da {
 cudaError_t launch_sched_meta(const SchedParams &p, cudaStream_t stream, bool pdl);
-cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const GqaParams &p, cudaStream_t stream, bool pdl);
+cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p,
+                       cudaStream_t stream, bool pdl);
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl);
 int mla_ctas_per_part();
@@ -147,14 +148,18 @@ EncodeTiledFn get_encode_tiled() {
     return fn;
 }
 
-// Both pools as one 5-D map over 8-byte elements:
+// The pools are described to the TMA unit as 8-byte elements (16 per 128-byte
+// box row): the shared-memory image is the same whatever the KV format.
+//
+// Both pools as one 5-D map:
 //   dim 0: 16 elements = 128 bytes          dim 1: NX halves of a head row (stride 128 B)
 //   dim 2: KV head (stride = row)           dim 3: global token = page*P + slot (stride row*H_kv)
 //   dim 4: pool, K or V (stride = distance between the two pools)
 // and a box {16, NX, 1, box_tok, 2}: one copy brings one page's K and V rows of
-// one head. base is the lower of the two pools.
-int make_kv_map(CUtensorMap *m, const void *base, uint64_t pool_dist, const da_desc *d, int elem_bytes,
-                int box_tok) {
+// one head. base is the lower of the two pools. With pool = nullptr, a 4-D map
+// of one pool (dims 0-3) and a box {16, NX, 1, box_tok}.
+int make_kv_map(CUtensorMap *m, const void *base, uint64_t pool_dist, bool two_pools, const da_desc *d,
+                int elem_bytes, int box_tok) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return DA_ERR_CUDA;
     const cuuint64_t row = (cuuint64_t)d->D_qk * elem_bytes;  // bytes of one token's head
@@ -164,9 +169,9 @@ int make_kv_map(CUtensorMap *m, const void *base, uint64_t pool_dist, const da_d
     cuuint64_t strides[4] = {128, row, row * d->H_kv, pool_dist};
     cuuint32_t box[5] = {128 / kTmaElemBytes, (cuuint32_t)nx, 1, (cuuint32_t)box_tok, 2};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 5, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, two_pools ? 5 : 4, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
@@ -270,14 +275,21 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         const int es = fp8 ? 1 : 2;
         const int P = desc->page_size;
         const int box_tok = P < kChunk ? P : kChunk;
-        // the two pools must be distinct, non-overlapping buffers
+        if ((int64_t)P * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+        // one map over both pools when their distance can be a tensor-map
+        // stride (a multiple of 16 below 2^40, not overlapping); else one per pool
         const uint64_t pool_bytes = (uint64_t)desc->num_pages * P * desc->H_kv * desc->D_qk * es;
         const uintptr_t ka = reinterpret_cast<uintptr_t>(k_pool), va = reinterpret_cast<uintptr_t>(v_pool);
         const uint64_t dist = ka > va ? (uint64_t)(ka - va) : (uint64_t)(va - ka);
-        if (dist < pool_bytes || dist >= (1ull << 40)) return DA_ERR_UNSUPPORTED;
-        if ((int64_t)P * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
-        CUtensorMap tkv;
-        if ((rc = make_kv_map(&tkv, ka < va ? k_pool : v_pool, dist, desc, es, box_tok))) return rc;
+        const bool combined = dist >= pool_bytes && dist < (1ull << 40);
+        CUtensorMap tkv, tv;
+        if (combined) {
+            if ((rc = make_kv_map(&tkv, ka < va ? k_pool : v_pool, dist, true, desc, es, box_tok))) return rc;
+            tv = tkv;
+        } else {
+            if ((rc = make_kv_map(&tkv, k_pool, 0, false, desc, es, box_tok))) return rc;
+            if ((rc = make_kv_map(&tv, v_pool, 0, false, desc, es, box_tok))) return rc;
+        }
         GqaParams p;
         p.q = q;
         p.block_table = block_table;
@@ -297,13 +309,14 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.box_tokens = box_tok;
         p.boxes_per_chunk = kChunk / box_tok;
         p.log2_box_tokens = box_tok == 8 ? 3 : box_tok == 16 ? 4 : box_tok == 32 ? 5 : 6;
-        p.kv_swap = va < ka ? 1 : 0;
+        p.kv_swap = (combined && va < ka) ? 1 : 0;
+        p.kv_combined = combined ? 1 : 0;
         p.splits = desc->splits;
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
         p.wait_limit_ns = kWaitLimitNs;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
-        if (launch_gqa(desc->D_qk, fp8, tkv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
+        if (launch_gqa(desc->D_qk, fp8, tkv, tv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     } else {
         MlaParams p;
         p.q = q;

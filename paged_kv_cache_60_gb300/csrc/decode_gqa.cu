@@ -165,7 +165,8 @@ __device__ __forceinline__ SegWalker make_walker(const MetaView &mv, const int4 
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_BLOCKS)
-    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ GqaParams p) {
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ GqaParams p) {
     using C = GqaCfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
     }
     if (warp == C::NCW && lane == 0) {
         prefetch_tmap(&tm_kv);
+        if (!p.kv_combined) prefetch_tmap(&tm_v);
     }
     __syncthreads();
     pdl_wait();
@@ -217,7 +219,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         // ------------------------------------------------------------ producer
         // Lane j < boxes_per_chunk owns box j of every chunk: one TMA per page
         // brings that page's K and V rows of head h (both pools, both 128-byte
-        // halves of a row, through one 5-D tensor map). Each lane keeps the
+        // halves of a row, through one 5-D tensor map; when the two pools are
+        // too far apart for one map, two 4-D maps and two copies). Each lane keeps the
         // page ids of its next four chunks in registers, loaded four chunks
         // ahead, arrives on the chunk's full barrier with its own byte count
         // and issues its own copy -- no shuffles, no load latency in the loop.
@@ -264,7 +267,12 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                         const int tok = (lc + k) * kChunk + lane * bt;
                         const int in_page = (P > kChunk) ? (tok % P) : 0;
                         uint8_t *st = smem + (size_t)stage * C::STAGE + lane * box_bytes;
-                        tma_load_5d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, 0, pol);
+                        if (p.kv_combined) {
+                            tma_load_5d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, 0, pol);
+                        } else {  // K map in tm_kv, V map in tm_v, same box image
+                            tma_load_4d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, pol);
+                            tma_load_4d(st + box_bytes / 2, &tm_v, &full[stage], 0, 0, h, pg * P + in_page, pol);
+                        }
                     }
                     ++i;
                 }
@@ -560,7 +568,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
 }
 
 template <int D, bool FP8>
-static cudaError_t launch_one(const CUtensorMap &tkv, const GqaParams &p, cudaStream_t stream, bool pdl) {
+static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
+                              bool pdl) {
     using C = GqaCfg<D, FP8>;
     auto kern = gqa_decode_kernel<D, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -575,13 +584,14 @@ static cudaError_t launch_one(const CUtensorMap &tkv, const GqaParams &p, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, tkv, p);
+    return cudaLaunchKernelEx(&cfg, kern, tkv, tv, p);
 }
 
-cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const GqaParams &p, cudaStream_t stream, bool pdl) {
-    if (!fp8 && D == 64) return launch_one<64, false>(tkv, p, stream, pdl);
-    if (!fp8 && D == 128) return launch_one<128, false>(tkv, p, stream, pdl);
-    if (fp8 && D == 128) return launch_one<128, true>(tkv, p, stream, pdl);
+cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p,
+                       cudaStream_t stream, bool pdl) {
+    if (!fp8 && D == 64) return launch_one<64, false>(tkv, tv, p, stream, pdl);
+    if (!fp8 && D == 128) return launch_one<128, false>(tkv, tv, p, stream, pdl);
+    if (fp8 && D == 128) return launch_one<128, true>(tkv, tv, p, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -79,6 +79,7 @@ struct GqaParams {
     int32_t B, H_kv, G, H_q, max_pages, num_pages, page_size, box_tokens, boxes_per_chunk;
     int32_t log2_box_tokens;       // box_tokens is 8, 16, 32 or 64
     int32_t kv_swap;               // 1: the V pool lies below the K pool (its rows come first in a box)
+    int32_t kv_combined;           // 1: one 5-D map covers both pools; 0: one 4-D map per pool
     int32_t splits, num_parts;
     float scale_log2;              // softmax_scale * log2(e)
     uint64_t wait_limit_ns;

@@ -249,3 +249,35 @@ def test_workload_parity(name, nsample):
     assert e_lse <= LSE_TOL, (name, e_lse)
     # every output of the full run is finite (poisoned slots never read)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+# ------------------------------------------------------------------ pool placement
+
+@pytest.mark.parametrize("kv", [KV_BF16, KV_FP8])
+def test_v_pool_below_k_pool(kv):
+    # one buffer, V in the lower half and K in the upper half
+    w = make_workload(_spec(kv_dtype=kv, lengths=[700, 90, 300]))
+    dw = DeviceWorkload(w)
+    both = torch.empty((2,) + tuple(w.k_pool.shape), dtype=w.k_pool.dtype, device="cuda")
+    both[0].copy_(dw.v_pool)
+    both[1].copy_(dw.k_pool)
+    dw.v_pool, dw.k_pool = both[0], both[1]
+    out, lse, _, _ = run(w, dw=dw)
+    ref_out, ref_lse = oracle.attend(w)
+    e_out, e_lse = max_err(out, lse, ref_out, ref_lse)
+    assert e_out <= OUT_TOL and e_lse <= LSE_TOL
+
+
+@pytest.mark.parametrize("kv", [KV_BF16, KV_FP8])
+def test_same_buffer_for_k_and_v(kv):
+    # K = V: the pools cannot share one tensor map, each gets its own
+    w = make_workload(_spec(kv_dtype=kv, lengths=[700, 90, 300]))
+    w.v_pool = w.k_pool
+    if w.k_scale is not None:
+        w.v_scale = w.k_scale
+    dw = DeviceWorkload(w)
+    dw.v_pool = dw.k_pool
+    out, lse, _, _ = run(w, dw=dw)
+    ref_out, ref_lse = oracle.attend(w)
+    e_out, e_lse = max_err(out, lse, ref_out, ref_lse)
+    assert e_out <= OUT_TOL and e_lse <= LSE_TOL
