@@ -22,7 +22,12 @@
  *      "Hopper 路径上 V 不做显式反量化": the KV scale multiplies the stored value)
  *   2  656-byte MLA token (FlashMLA page, section "数据加载"): 512 e4m3 values,
  *      4 fp32 scales (one per 128 values), 64 bf16 RoPE values. K is the 576
- *      values (dequantised NoPE then RoPE); V is the first D_v of them.
+ *      values (dequantised NoPE then RoPE); V is the first D_v of them. The
+ *      page's dequantisation goes FP8 -> half -> float32, times the float32
+ *      scale, -> bfloat16 ("计算环节一"); the products then run on those
+ *      bfloat16 values ("数据加载"). So a NoPE value here is
+ *      bf16(float32(e4m3) * scale): the float32 product, rounded to nearest
+ *      even, then rounded to bf16 (nearest even).
  *   3  float64 (pins only)
  *
  * Split reference: the same sum restricted to a token range [t0, t1), giving a
@@ -82,6 +87,17 @@ static double f32_at(const uint8_t *p)
     return (double)f;
 }
 
+/* Nearest bf16 (ties to even) of a float32, for finite values. */
+static double bf16_round(float f)
+{
+    uint32_t w;
+    memcpy(&w, &f, 4);
+    uint32_t keep = w >> 16, rest = w & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1;
+    return ref_bf16_value((uint16_t)keep);
+}
+
 /* Decode logical token t of (b, h) into k[D_qk] and v[D_v]. Returns 0, or -1
  * if the block table points outside the pool. */
 static int gather_token(const ref_desc *d, const void *k_pool, const void *v_pool,
@@ -108,7 +124,7 @@ static int gather_token(const ref_desc *d, const void *k_pool, const void *v_poo
     } else if (d->kv_dtype == REF_MLA656) {
         const uint8_t *r = (const uint8_t *)k_pool + row * 656;
         for (int i = 0; i < 512; i++)
-            k[i] = ref_e4m3_value(r[i]) * f32_at(r + 512 + 4 * (i / 128));
+            k[i] = bf16_round((float)(ref_e4m3_value(r[i]) * f32_at(r + 512 + 4 * (i / 128))));
         for (int i = 0; i < 64; i++) {
             uint16_t bits = (uint16_t)(r[528 + 2 * i] | (r[528 + 2 * i + 1] << 8));
             k[512 + i] = ref_bf16_value(bits);

@@ -290,10 +290,11 @@ def test_mla656_equals_predequantised(oracle_lib):
                         kv_dtype=KV_MLA656, lengths=[21, 9], extra_pages=2, seed=5)
     w = make_workload(spec)
     raw = w.k_pool.reshape(-1, 656)
-    nope = raw[:, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
-    scales = raw[:, 512:528].contiguous().view(torch.float32).to(torch.float64)
     rope = raw[:, 528:].contiguous().view(torch.bfloat16).to(torch.float64)
-    k = torch.cat([nope * scales.repeat_interleave(128, dim=1), rope], dim=1)
+    # the page's chain: float32 value times float32 scale, then bfloat16
+    nope32 = raw[:, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+    deq = (nope32 * raw[:, 512:528].contiguous().view(torch.float32).repeat_interleave(128, dim=1))
+    k = torch.cat([deq.to(torch.bfloat16).to(torch.float64), rope], dim=1)
     kd = k.reshape(w.num_pages, 8, 1, 576)
     vd = k[:, :512].reshape(w.num_pages, 8, 1, 512)
     o1, l1 = oracle.attend(w)
@@ -339,3 +340,18 @@ def test_query_head_order_h_times_g_plus_g(oracle_lib):
             hq = h * spec.G + g
             assert torch.allclose(out[0, hq], torch.full((8,), float(100 * h + hq), dtype=torch.float64),
                                   atol=1e-9, rtol=0)
+
+
+def test_mla_dequant_rounds_like_torch_float32_then_bf16(oracle_lib):
+    # single-token requests: out equals the token's dequantised V row exactly
+    spec = WorkloadSpec(name="m1", B=3, H_kv=1, G=2, D_qk=576, D_v=512, page_size=8,
+                        kv_dtype=KV_MLA656, lengths=[1, 1, 1], seed=9)
+    w = make_workload(spec)
+    out, _ = oracle.attend(w)
+    for b in range(3):
+        page = int(w.block_table[b, 0])
+        raw = w.k_pool[page, 0, 0]
+        v32 = raw[:512].contiguous().view(torch.float8_e4m3fn).to(torch.float32)
+        sc = raw[512:528].contiguous().view(torch.float32).repeat_interleave(128)
+        want = (v32 * sc).to(torch.bfloat16).to(torch.float64)
+        assert torch.equal(out[b, 0], want) and torch.equal(out[b, 1], want)
