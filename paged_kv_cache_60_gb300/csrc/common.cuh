@@ -74,6 +74,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Non-blocking test of phase completion.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait that ignores the abort flag (for draining work already issued).
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_ns();
@@ -173,6 +188,19 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 
 // ------------------------------------------------------------------ conversions
 // Two e4m3 (low byte -> low half) to two f16 (exact).
+// 16-byte read-only global load that does not allocate in L1 (streamed data).
+__device__ __forceinline__ uint4 ldg_stream16(const void *ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+__device__ __forceinline__ float ldg_stream4f(const void *ptr) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     uint32_t y;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));

@@ -144,42 +144,33 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // Two cursors walk the same chunk sequence: one issues S = Q K^T,
+            // the other O^T += V^T P^T. Whichever is ready goes first (the
+            // product for P first, since the next chunk's tile waits on it);
+            // the barriers keep S at most two chunks ahead.
             constexpr uint32_t IDESC_QK = umma_idesc_bf16(64, 64, 0, 0);
             constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 64, 1, 0);
-            SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
-            Seg sg;
-            int ic = 0, seg = 0;
-            bool ok = true;
-            auto qk = [&](int cur) -> bool {
-                const int kb = cur & 1;
-                if (!mbar_wait_bounded(&kfull[kb], (cur >> 1) & 1, abort_flag, p.wait_limit_ns)) return false;
-                if (!mbar_wait_bounded(&sfree[kb], ((cur >> 1) & 1) ^ 1, abort_flag, p.wait_limit_ns)) return false;
-                tc_fence_after();
-#pragma unroll 4
-                for (int ks = 0; ks < DQK / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * SLICE + (ks & 3) * 32;
-                    umma_bf16(tmem + S_COL + 64 * kb, umma_desc(q_addr + off, 16, 1024),
-                              umma_desc(k_addr[kb] + off, 16, 1024), IDESC_QK, ks > 0);
+            SegWalker wq = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
+            SegWalker wp = wq;
+            auto next_seg = [](SegWalker &w, int &n) -> bool {
+                Seg g;
+                while (w.next(g)) {
+                    n = g.lc1 - g.lc0;
+                    if (n > 0) return true;
                 }
-                umma_commit(&sfull[kb]);
-                return true;
+                return false;
             };
-            while (ok && wk.next(sg)) {
-                const int n = sg.lc1 - sg.lc0;
-                if (n == 0) continue;
-                if (!(ok = mbar_wait_bounded(qfull, seg & 1, abort_flag, p.wait_limit_ns))) break;
-                if (!(ok = qk(ic))) break;
-                for (int c = 0; c < n && ok; ++c) {
-                    const int cur = ic + c, kb = cur & 1;
-                    if (c + 1 < n) {
-                        if (!(ok = qk(cur + 1))) break;
-                    } else {
-                        umma_commit(qfree);  // Q may be replaced once these products complete
-                    }
-                    if (!(ok = mbar_wait_bounded(pfull, cur & 1, abort_flag, p.wait_limit_ns))) break;
-                    if (c == 0 && seg > 0 &&
-                        !(ok = mbar_wait_bounded(ofree, (seg - 1) & 1, abort_flag, p.wait_limit_ns)))
-                        break;
+            int nq = 0, np = 0;
+            bool q_more = next_seg(wq, nq), p_more = next_seg(wp, np);
+            int qc = 0, pc = 0, qcur = 0, pcur = 0, qseg = 0, pseg = 0;
+            bool ok = true;
+            uint64_t t_idle = 0;
+            uint32_t spins = 0;
+            while (q_more || p_more) {
+                bool issued = false;
+                if (p_more && pcur < qcur && mbar_test(pfull, pcur & 1) &&
+                    (pc != 0 || pseg == 0 || mbar_test(ofree, (pseg - 1) & 1))) {
+                    const int kb = pcur & 1;
                     tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -187,16 +178,50 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                         for (int kt = 0; kt < kChunk / 16; ++kt) {
                             const uint64_t a = umma_desc(k_addr[kb] + 2 * j * SLICE + kt * 2048, SLICE, 1024);
                             const uint64_t b = umma_desc(p_addr + kt * 32, 16, 1024);
-                            umma_bf16(tmem + O_COL + 64 * j, a, b, IDESC_PV, !(c == 0 && kt == 0));
+                            umma_bf16(tmem + O_COL + 64 * j, a, b, IDESC_PV, !(pc == 0 && kt == 0));
                         }
                     }
                     umma_commit(&kempty[kb]);
                     umma_commit(pfree);
+                    if (pc == np - 1) umma_commit(ofull);
+                    ++pcur;
+                    if (++pc == np) {
+                        pc = 0;
+                        ++pseg;
+                        p_more = next_seg(wp, np);
+                    }
+                    issued = true;
+                } else if (q_more && (qc != 0 || mbar_test(qfull, qseg & 1)) &&
+                           mbar_test(&kfull[qcur & 1], (qcur >> 1) & 1) &&
+                           mbar_test(&sfree[qcur & 1], ((qcur >> 1) & 1) ^ 1)) {
+                    const int kb = qcur & 1;
+                    tc_fence_after();
+#pragma unroll 4
+                    for (int ks = 0; ks < DQK / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * SLICE + (ks & 3) * 32;
+                        umma_bf16(tmem + S_COL + 64 * kb, umma_desc(q_addr + off, 16, 1024),
+                                  umma_desc(k_addr[kb] + off, 16, 1024), IDESC_QK, ks > 0);
+                    }
+                    umma_commit(&sfull[kb]);
+                    if (qc == nq - 1) umma_commit(qfree);  // Q may be replaced once these complete
+                    ++qcur;
+                    if (++qc == nq) {
+                        qc = 0;
+                        ++qseg;
+                        q_more = next_seg(wq, nq);
+                    }
+                    issued = true;
                 }
-                if (!ok) break;
-                umma_commit(ofull);
-                ic += n;
-                ++seg;
+                if (issued) {
+                    spins = 0;
+                } else if ((++spins & 63) == 0) {
+                    const uint64_t now = global_ns();
+                    if (spins == 64) t_idle = now;
+                    if (*abort_flag || now - t_idle > p.wait_limit_ns) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             if (!ok) {
                 atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
@@ -204,12 +229,16 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             }
             // every product issued here has completed before the TMEM goes away
             umma_commit(qfree);
-            mbar_wait_timed(qfree, (seg & 1), 100000000ull);
+            mbar_wait_timed(qfree, (qseg & 1), 100000000ull);
         }
     } else if (warp >= 5) {
         // ------------------------------------------------------------ dequantise K/V tokens, load Q
+        // Warp dw owns tokens 8 dw .. 8 dw + 7 of every chunk. Per token, lane l
+        // reads NoPE bytes 16 l .. 16 l + 15 (one 512-byte coalesced load per
+        // warp), lanes 0-7 the RoPE part and lanes 0-3 the four scales; all
+        // loads of a chunk are in flight while the warp waits for its buffer.
         const int dt = threadIdx.x - 5 * 32;  // 0 .. 255
-        const int tok = dt >> 2, q4 = dt & 3;  // 4 threads per token; q4 = scale block
+        const int dw = warp - 5;
         SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
         Seg sg;
         int ic = 0, seg = 0;
@@ -233,43 +262,50 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
             for (int c = 0; c < n && ok; ++c) {
                 const int cur = ic + c, kb = cur & 1;
-                const int t = (sg.lc0 + c) * kChunk + tok;
-                const uint8_t *row = nullptr;
-                if (t < sg.L) {
-                    const int pg = bt_row[t / p.page_size];
+                const int t0 = (sg.lc0 + c) * kChunk + 8 * dw;  // first of this warp's 8 tokens
+                // the 8 tokens lie in one page (page sizes are multiples of 8)
+                const uint8_t *rows = nullptr;
+                if (t0 < sg.L) {
+                    const int pg = bt_row[t0 / p.page_size];
                     if (pg < 0 || pg >= p.num_pages) {
-                        atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
-                        p.meta.header[kHErrorDetail] = pg;
+                        if (lane == 0) {
+                            atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
+                            p.meta.header[kHErrorDetail] = pg;
+                        }
                     } else {
-                        row = p.pool + ((size_t)pg * p.page_size + t % p.page_size) * ROW_BYTES;
+                        rows = p.pool + ((size_t)pg * p.page_size + t0 % p.page_size) * ROW_BYTES;
                     }
                 }
-                uint4 raw[8], rope[2];
-                float scale = 0.f;
-                if (row) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(row + 128 * q4);
+                const int nv = rows ? min(8, sg.L - t0) : 0;  // valid tokens of the 8
+                uint4 nope[8], rope[8];
+                float sc[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) raw[k] = src[k];
-                    const uint4 *rsrc = reinterpret_cast<const uint4 *>(row + 528);
-                    rope[0] = rsrc[2 * q4];
-                    rope[1] = rsrc[2 * q4 + 1];
-                    scale = reinterpret_cast<const float *>(row + 512)[q4];
+                for (int i = 0; i < 8; ++i) {
+                    nope[i] = make_uint4(0u, 0u, 0u, 0u);
+                    rope[i] = nope[i];
+                    sc[i] = 0.f;
+                    if (i < nv) {
+                        const uint8_t *r = rows + i * ROW_BYTES;
+                        nope[i] = ldg_stream16(r + 16 * lane);
+                        if (lane < 8) rope[i] = ldg_stream16(r + 528 + 16 * lane);
+                        if (lane < 4) sc[i] = ldg_stream4f(r + 512 + 4 * lane);
+                    }
                 }
                 if (!(ok = mbar_wait_warp(&kempty[kb], ((cur >> 1) & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
                 uint8_t *kt = smem + (kb ? OFF_K1 : OFF_K0);
+                // lane l's 16 values go to slice l / 4, 16-byte chunks 2 (l % 4) and 2 (l % 4) + 1;
+                // half the lanes store their upper chunk first so each store touches all banks
+                const int sl = lane >> 2, cA = 2 * (lane & 3) + ((lane >> 2) & 1), cB = cA ^ 1;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                    if (row) dequant16(raw[k], scale, lo, hi);
-                    // values 128 q4 + 16 k .. +15: slice 2 q4 + k / 4, 16-byte chunks 2 (k % 4), +1
-                    const int sl = 2 * q4 + (k >> 2), c16 = 2 * (k & 3);
-                    *reinterpret_cast<uint4 *>(kt + sl * SLICE + swz(tok, c16)) = lo;
-                    *reinterpret_cast<uint4 *>(kt + sl * SLICE + swz(tok, c16 + 1)) = hi;
-                }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint4 v = row ? rope[e] : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4 *>(kt + 8 * SLICE + swz(tok, 2 * q4 + e)) = v;
+                for (int i = 0; i < 8; ++i) {
+                    const int tok = 8 * dw + i;
+                    const float scale = __shfl_sync(0xffffffffu, sc[i], lane >> 3);
+                    uint4 lo, hi;
+                    dequant16(nope[i], scale, lo, hi);
+                    const bool swap = (lane >> 2) & 1;
+                    *reinterpret_cast<uint4 *>(kt + sl * SLICE + swz(tok, cA)) = swap ? hi : lo;
+                    *reinterpret_cast<uint4 *>(kt + sl * SLICE + swz(tok, cB)) = swap ? lo : hi;
+                    if (lane < 8) *reinterpret_cast<uint4 *>(kt + 8 * SLICE + swz(tok, lane)) = rope[i];
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
