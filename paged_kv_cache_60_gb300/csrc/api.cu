@@ -18,6 +18,7 @@ cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl);
 int mla_ctas_per_part();
 bool mla_kernel_available();
+int mla_max_parts();
 }  // namespace da
 
 using namespace da;
@@ -70,6 +71,13 @@ int resolve_sms(const da_desc *d, int *nsm) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
     if (cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DA_ERR_CUDA;
+    if (is_mla(d)) {
+        // the latent-token kernel runs as two-CTA clusters: count the SMs that
+        // can hold one at the same time
+        const int clusters = mla_max_parts();
+        if (clusters < 1) return DA_ERR_CUDA;
+        if (2 * clusters < *nsm) *nsm = 2 * clusters;
+    }
     return DA_OK;
 }
 

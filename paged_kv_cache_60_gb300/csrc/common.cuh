@@ -260,6 +260,72 @@ __device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
 }
 
 
+// ------------------------------------------------------------------ clusters (distributed shared memory)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, const uint4 &v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
+// earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Warp-wide bounded wait on a phase completed by another CTA's arrivals.
+__device__ __forceinline__ bool mbar_wait_warp_cluster(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                                       uint64_t limit_ns) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_cluster(bar, parity))) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_cluster(bar, parity))) return true;
+        if ((it & 15) == 15) {
+            int stop = (*abort != 0) || (global_ns() - t0 > limit_ns);
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+// 16-byte store into another CTA's shared memory that counts its bytes on
+// that CTA's mbarrier (complete_tx) instead of ordering through a fence.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, const uint4 &v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     caddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cbar)
+                 : "memory");
+}
+// Arrive on another CTA's mbarrier without ordering earlier memory accesses
+// (for acknowledgements whose loads have already been consumed).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05 (5th-gen tensor cores, TMEM)
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), version 1, layout type (2 = 128-byte swizzle).
@@ -283,6 +349,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+// Same, with the A operand read from tensor memory (rows in lanes, K packed
+// two bf16 per 32-bit column).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 bool accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
         : "memory");
 }
 // Arrive once on `bar` when every MMA issued so far by this thread has completed.

@@ -1,31 +1,36 @@
 // Split-KV decode kernel for the 656-byte FP8 latent token (MQA: 128 query
 // heads share one KV head; D_qk = 576, D_v = 512), on the 5th-generation
-// tensor cores (tcgen05, accumulators in tensor memory).
+// tensor cores (tcgen05, accumulators and one operand in tensor memory).
 //
 // The token format is the FlashMLA page's ("FlashMLA 注意力内核源码走读", section
 // "数据加载"): 512 e4m3 values with one fp32 scale per 128 of them, then 64
 // bf16 RoPE values; K is the 576 dequantised values and V their first 512.
-// Dequantisation goes to bf16 and the products run in bf16 with fp32
-// accumulation, as that section describes.
+// Dequantisation goes to bf16 (exact e4m3 value in fp32, times the scale, ->
+// bf16) and the products run in bf16 with fp32 accumulation, as that section
+// describes.
 //
-// Work split: two CTAs per part, each owning 64 of the 128 query heads. The
-// output of 128 heads x 512 values in fp32 would fill a whole SM's tensor
-// memory, so it is split by head across the pair; each CTA dequantises the
-// part's tokens itself (the KV bytes are read from HBM once and from L2 twice).
+// Work split: a cluster of two CTAs (two SMs) per part. Both hold all 128
+// query heads, so every MMA has 128 rows (one per head). CTA r holds dims
+// [256 r, 256 r + 320) of each latent row:
+//   S_r = Q[:, 288 r : 288 r + 288] K[:, same]^T   M = 128 heads, N = 64 tokens, 18 MMAs,
+//                                                 Q read from tensor memory
+//   the two partial S are swapped through distributed shared memory and added
+//   (fp32 addition commutes, so both CTAs hold the same S bit for bit and take
+//   the same softmax decisions without further exchange);
+//   O[:, 256 r : 256 r + 256] += P V               M = 128 heads, N = 256 dims, 4 MMAs,
+//                                                 P read from tensor memory
+// So each CTA dequantises 320 of the 576 values of a token, and O (128 heads x
+// 512 fp32) is split by value dim across the pair's tensor memories.
 //
-// Per 64-token chunk:
-//   S  = Q K^T   M = 64 heads, N = 64 tokens, K = 576   (S in TMEM, double buffered)
-//   softmax      one thread per head: running max m, sum l, exp2, P -> shared memory (bf16)
-//   O^T += V^T P^T  M = 128 (four blocks of V's 512 columns), N = 64 heads, K = 64 tokens
-// V^T is read straight from the dequantised K tile through an MN-major
-// descriptor, so the tile is written once. The running max is re-based only
-// when it grows by more than 2^8 (then O^T columns are rescaled in TMEM);
-// otherwise P values stay below 256 and the sums are exact to fp32 rounding.
-// (Online softmax: attention pipeline page, section 三; exp via exp2: section 一.)
+// Softmax (one thread per head, which also owns that head's row of S, P and
+// O in tensor memory): running max m, sum l, exp2; the max is re-based only
+// when it grows by more than 2^8 (then the thread rescales its O row);
+// otherwise P values stay below 256. (Online softmax: attention pipeline page,
+// section 三; exp via exp2: section 一.)
 //
 // Roles (416 threads): warp 0 issues MMAs (one lane) and owns the TMEM
-// allocation; warps 1-4 run the softmax and the epilogue (TMEM lane quadrant
-// = warp % 4); warps 5-12 dequantise tokens and load Q.
+// allocation; warps 1-4 load Q, run the softmax and the epilogue (TMEM lane
+// quadrant = warp % 4); warps 5-12 dequantise tokens into a four-deep ring.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -36,97 +41,125 @@
 namespace da {
 
 namespace mla {
-constexpr int HEADS = 64;                  // query heads per CTA
+constexpr int HQ = 128;                    // query heads, all of them in each CTA
 constexpr int DQK = 576, DV = 512;
-constexpr int NSL = DQK / 64;              // 64-column slices of a row (9)
-constexpr int SLICE = kChunk * 128;        // one slice of a 64-row tile (8 KB)
-constexpr int TILE = NSL * SLICE;          // 64 rows x 576 bf16 (72 KB)
+constexpr int WIN = 320;                   // dims of a latent row held by one CTA: [256 r, 256 r + 320)
+constexpr int WSL = WIN / 64;              // 64-dim slices of the window (5)
+constexpr int UNITS = WIN / 16;            // 16-value units per token row (20)
+constexpr int KSTEPS = 18;                 // 288 contraction dims per CTA, 16 per MMA
+constexpr int KSLICE = kChunk * 128;       // one slice of a 64-token tile (8 KB)
+constexpr int KTILE = WSL * KSLICE;        // 40 KB
+constexpr int NK = 4;                      // depth of the dequantised-tile ring
 constexpr int ROW_BYTES = 656;
-constexpr int OFF_Q = 0;
-constexpr int OFF_K0 = TILE;
-constexpr int OFF_K1 = 2 * TILE;
-constexpr int OFF_P = 3 * TILE;
-constexpr int OFF_MISC = OFF_P + HEADS * 128;
-// misc: 14 mbarriers, tmem base, abort flag, per-head alpha / l / m
+constexpr int XROW = kChunk * 4 + 16;      // exchange-buffer row: 64 fp32 + 16 bytes of padding
+constexpr int OFF_K = 0;                   // NK tiles
+constexpr int OFF_X = NK * KTILE;          // the peer's partial S: 128 heads x 64 tokens fp32
+constexpr int OFF_MISC = OFF_X + HQ * XROW;
+// misc: mbarriers, tmem base, abort flag
+constexpr int NBARS = 2 * NK + 10;
 constexpr int OFF_BARS = OFF_MISC;
-constexpr int OFF_TMEM = OFF_BARS + 14 * 8;
+constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_ALPHA = OFF_ABORT + 12;
-constexpr int OFF_L = OFF_ALPHA + HEADS * 4;
-constexpr int OFF_M = OFF_L + HEADS * 4;
-constexpr int SMEM = OFF_M + HEADS * 4 + 1024;  // + alignment slack
+constexpr int SMEM = OFF_ABORT + 12 + 1024;  // + alignment slack
 constexpr int THREADS = 13 * 32;
-constexpr int SM_WARPS = 4, DQ_WARPS = 8;
+constexpr int SM_THREADS = 128, DQ_WARPS = 8;
+// tensor memory (512 columns x 128 lanes; lane = head)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;              // two S buffers: columns 0 and 64
-constexpr uint32_t O_COL = 128;            // O^T blocks j = 0..3 at 128 + 64 j
+constexpr uint32_t O_COL = 0;              // O: 256 fp32 value dims
+constexpr uint32_t S_COL = 256;            // S: 64 fp32 tokens
+constexpr uint32_t Q_COL = 320;            // Q: 288 bf16 dims, two per column (144 columns)
+constexpr uint32_t P_COL = 464;            // P: 64 bf16 tokens, two per column (32 columns)
 constexpr float RESCALE_LOG2 = 8.f;        // re-base the max when it grows by more than 2^8
 static_assert(SMEM <= 232448, "shared memory budget");
+static_assert(P_COL + 32 <= TMEM_COLS, "tensor memory budget");
+static_assert(KTILE % 1024 == 0, "1024-byte aligned operand tiles");
 }  // namespace mla
 
 constexpr float kLn2Mla = 0.6931471805599453f;
 
 __device__ __forceinline__ uint32_t swz(int row, int c16) { return (uint32_t)(row * 128 + ((c16 ^ (row & 7)) << 4)); }
 
-// 16 e4m3 values times `scale`, as 16 bf16 (two 16-byte words).
+// Exact e4m3 -> fp32 without the conversion pipe: the sign, exponent and
+// mantissa bits of the code are moved to the fp32 sign, the low exponent bits
+// and the top mantissa bits, which gives the value times 2^-120 (a subnormal
+// fp32 for e4m3 subnormals); one multiply by 2^120 (no flush to zero) makes it
+// exact. The NaN codes (0x7f, 0xff) decode to +-480 here; the tokens a decode
+// step reads never hold them.
+__device__ __forceinline__ float e4m3_from_bits(uint32_t fbits) {
+    float r;
+    asm("mul.rn.f32 %0, %1, 0f7B800000;" : "=f"(r) : "f"(__uint_as_float(fbits)));  // x 2^120
+    return r;
+}
+__device__ __forceinline__ float mul_rn(float a, float b) {
+    float r;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// 16 e4m3 values times `scale` (fp32 product, then bf16 round to nearest even),
+// as 16 bf16 (two 16-byte words).
 __device__ __forceinline__ void dequant16(const uint4 v, float scale, uint4 &lo, uint4 &hi) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint32_t h01 = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffff));
-        const uint32_t h23 = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
-        o[2 * k] = pack_bf16(f01.x * scale, f01.y * scale);
-        o[2 * k + 1] = pack_bf16(f23.x * scale, f23.y * scale);
+        const uint32_t x = w[k];
+        const float f0 = e4m3_from_bits(((x << 20) & 0x07f00000u) | ((x << 24) & 0x80000000u));
+        const float f1 = e4m3_from_bits(((x << 12) & 0x07f00000u) | ((x << 16) & 0x80000000u));
+        const float f2 = e4m3_from_bits(((x << 4) & 0x07f00000u) | ((x << 8) & 0x80000000u));
+        const float f3 = e4m3_from_bits(((x >> 4) & 0x07f00000u) | (x & 0x80000000u));
+        o[2 * k] = pack_bf16(mul_rn(f0, scale), mul_rn(f1, scale));
+        o[2 * k + 1] = pack_bf16(mul_rn(f2, scale), mul_rn(f3, scale));
     }
     lo = make_uint4(o[0], o[1], o[2], o[3]);
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
+
+// Position of 16-byte chunk i of head h's 256-byte row in the exchange buffer:
+// rows are padded to 272 bytes, so a warp's stores and loads spread over all
+// banks while the chunk offsets stay constants.
+__device__ __forceinline__ uint32_t xoff(int h, int i) { return (uint32_t)(h * mla::XROW + 16 * i); }
 
 __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __grid_constant__ MlaParams p) {
     using namespace mla;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
-    uint64_t *kfull = bars + 0, *kempty = bars + 2, *sfull = bars + 4, *sfree = bars + 6;
-    uint64_t *pfull = bars + 8, *pfree = bars + 9, *ofull = bars + 10, *ofree = bars + 11;
-    uint64_t *qfull = bars + 12, *qfree = bars + 13;
+    uint64_t *kfull = bars, *kempty = bars + NK;
+    uint64_t *sfull = bars + 2 * NK, *sfree = sfull + 1, *pfull = sfull + 2, *pfree = sfull + 3;
+    uint64_t *ofull = sfull + 4, *ofree = sfull + 5, *qfull = sfull + 6, *qfree = sfull + 7;
+    uint64_t *xfull = sfull + 8, *xfree = sfull + 9;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_ABORT);
-    float *alpha_sm = reinterpret_cast<float *>(smem + OFF_ALPHA);
-    float *l_sm = reinterpret_cast<float *>(smem + OFF_L);
-    float *m_sm = reinterpret_cast<float *>(smem + OFF_M);
-    const uint32_t q_addr = smem_u32(smem + OFF_Q);
-    const uint32_t k_addr[2] = {smem_u32(smem + OFF_K0), smem_u32(smem + OFF_K1)};
-    const uint32_t p_addr = smem_u32(smem + OFF_P);
+    const uint32_t k_base = smem_u32(smem + OFF_K);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int part = blockIdx.x, hh = blockIdx.y;  // head half: heads [64 hh, 64 hh + 64)
+    const int part = blockIdx.x;
+    const uint32_t rank = cluster_ctarank();  // 0 or 1: which window of the latent row
+    const uint32_t peer = rank ^ 1u;
 
     if (threadIdx.x == 0) {
-        mbar_init(&kfull[0], DQ_WARPS);
-        mbar_init(&kfull[1], DQ_WARPS);
-        mbar_init(&kempty[0], 1);
-        mbar_init(&kempty[1], 1);
-        mbar_init(&sfull[0], 1);
-        mbar_init(&sfull[1], 1);
-        mbar_init(&sfree[0], SM_WARPS);
-        mbar_init(&sfree[1], SM_WARPS);
-        mbar_init(pfull, SM_WARPS);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&kfull[i], DQ_WARPS);
+            mbar_init(&kempty[i], 1);
+        }
+        mbar_init(sfull, 1);
+        mbar_init(sfree, SM_THREADS / 32);
+        mbar_init(pfull, SM_THREADS / 32);
         mbar_init(pfree, 1);
         mbar_init(ofull, 1);
-        mbar_init(ofree, SM_WARPS);
-        mbar_init(qfull, DQ_WARPS);
+        mbar_init(ofree, SM_THREADS / 32);
+        mbar_init(qfull, SM_THREADS / 32);
         mbar_init(qfree, 1);
+        mbar_init(xfull, 1);  // armed locally; the peer's stores count their bytes
+        mbar_init(xfree, SM_THREADS / 32);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // the peer's barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_wait();
@@ -140,16 +173,18 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     const int max_len = p.max_pages * p.page_size;
 
     if (!meta_ok) {
-        if (threadIdx.x == 0) atomicOr(&p.meta.header[kHError], DA_DEV_META_MISMATCH);
+        if (threadIdx.x == 0 && rank == 0) atomicOr(&p.meta.header[kHError], DA_DEV_META_MISMATCH);
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             // Two cursors walk the same chunk sequence: one issues S = Q K^T,
-            // the other O^T += V^T P^T. Whichever is ready goes first (the
-            // product for P first, since the next chunk's tile waits on it);
-            // the barriers keep S at most two chunks ahead.
-            constexpr uint32_t IDESC_QK = umma_idesc_bf16(64, 64, 0, 0);
-            constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 64, 1, 0);
+            // the other O += P V. The product for P goes first when it is
+            // ready (the softmax of the next chunk waits on it); S is issued
+            // in two halves so that a P that becomes ready meanwhile is not
+            // queued behind a whole S.
+            constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 64, 0, 0);
+            constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 256, 0, 1);
+            const int ks0 = 2 * (int)rank;  // first 16-dim step of this CTA's 288 contraction dims in its window
             SegWalker wq = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
             SegWalker wp = wq;
             auto next_seg = [](SegWalker &w, int &n) -> bool {
@@ -163,25 +198,22 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             int nq = 0, np = 0;
             bool q_more = next_seg(wq, nq), p_more = next_seg(wp, np);
             int qc = 0, pc = 0, qcur = 0, pcur = 0, qseg = 0, pseg = 0;
+            int qhalf = 0;  // 0: next S starts fresh; 1: its first half is issued
+            int qdone = 0;  // chunks whose S is fully issued
             bool ok = true;
             uint64_t t_idle = 0;
             uint32_t spins = 0;
             while (q_more || p_more) {
                 bool issued = false;
-                if (p_more && pcur < qcur && mbar_test(pfull, pcur & 1) &&
+                if (p_more && pcur < qdone && mbar_test(pfull, pcur & 1) &&
                     (pc != 0 || pseg == 0 || mbar_test(ofree, (pseg - 1) & 1))) {
-                    const int kb = pcur & 1;
+                    const uint32_t kb = k_base + (pcur % NK) * KTILE;
                     tc_fence_after();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                        for (int kt = 0; kt < kChunk / 16; ++kt) {
-                            const uint64_t a = umma_desc(k_addr[kb] + 2 * j * SLICE + kt * 2048, SLICE, 1024);
-                            const uint64_t b = umma_desc(p_addr + kt * 32, 16, 1024);
-                            umma_bf16(tmem + O_COL + 64 * j, a, b, IDESC_PV, !(pc == 0 && kt == 0));
-                        }
-                    }
-                    umma_commit(&kempty[kb]);
+                    for (int kt = 0; kt < kChunk / 16; ++kt)
+                        umma_bf16_tmem_a(tmem + O_COL, tmem + P_COL + 8 * kt, umma_desc(kb + kt * 2048, KSLICE, 1024),
+                                         IDESC_PV, !(pc == 0 && kt == 0));
+                    umma_commit(&kempty[pcur % NK]);
                     umma_commit(pfree);
                     if (pc == np - 1) umma_commit(ofull);
                     ++pcur;
@@ -191,24 +223,31 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                         p_more = next_seg(wp, np);
                     }
                     issued = true;
-                } else if (q_more && (qc != 0 || mbar_test(qfull, qseg & 1)) &&
-                           mbar_test(&kfull[qcur & 1], (qcur >> 1) & 1) &&
-                           mbar_test(&sfree[qcur & 1], ((qcur >> 1) & 1) ^ 1)) {
-                    const int kb = qcur & 1;
-                    tc_fence_after();
-#pragma unroll 4
-                    for (int ks = 0; ks < DQK / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * SLICE + (ks & 3) * 32;
-                        umma_bf16(tmem + S_COL + 64 * kb, umma_desc(q_addr + off, 16, 1024),
-                                  umma_desc(k_addr[kb] + off, 16, 1024), IDESC_QK, ks > 0);
+                } else if (q_more && (qhalf == 1 ||
+                                      ((qc != 0 || mbar_test(qfull, qseg & 1)) &&
+                                       mbar_test(&kfull[qcur % NK], (qcur / NK) & 1) &&
+                                       mbar_test(sfree, (qcur & 1) ^ 1)))) {
+                    const uint32_t kb = k_base + (qcur % NK) * KTILE;
+                    if (qhalf == 0) tc_fence_after();
+                    const int i0 = qhalf * (KSTEPS / 2);
+#pragma unroll
+                    for (int i = i0; i < i0 + KSTEPS / 2; ++i) {
+                        const int ks = ks0 + i;
+                        umma_bf16_tmem_a(tmem + S_COL, tmem + Q_COL + 8 * i,
+                                         umma_desc(kb + (ks >> 2) * KSLICE + (ks & 3) * 32, 16, 1024), IDESC_QK, i > 0);
                     }
-                    umma_commit(&sfull[kb]);
-                    if (qc == nq - 1) umma_commit(qfree);  // Q may be replaced once these complete
-                    ++qcur;
-                    if (++qc == nq) {
-                        qc = 0;
-                        ++qseg;
-                        q_more = next_seg(wq, nq);
+                    if (qhalf == 0) {
+                        qhalf = 1;
+                    } else {
+                        qhalf = 0;
+                        umma_commit(sfull);
+                        if (qc == nq - 1) umma_commit(qfree);  // Q may be replaced once these complete
+                        qdone = ++qcur;
+                        if (++qc == nq) {
+                            qc = 0;
+                            ++qseg;
+                            q_more = next_seg(wq, nq);
+                        }
                     }
                     issued = true;
                 }
@@ -232,142 +271,179 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             mbar_wait_timed(qfree, (qseg & 1), 100000000ull);
         }
     } else if (warp >= 5) {
-        // ------------------------------------------------------------ dequantise K/V tokens, load Q
-        // Warp dw owns tokens 8 dw .. 8 dw + 7 of every chunk. Per token, lane l
-        // reads NoPE bytes 16 l .. 16 l + 15 (one 512-byte coalesced load per
-        // warp), lanes 0-7 the RoPE part and lanes 0-3 the four scales; all
-        // loads of a chunk are in flight while the warp waits for its buffer.
+        // ------------------------------------------------------------ dequantise this CTA's window
+        // A token row of the window is 20 units of 16 values. Thread dt takes
+        // units dt + 256 i (i < 5) of the chunk's 64 x 20, so a warp's loads
+        // cover contiguous bytes of one or two rows. Rank 0's units are NoPE
+        // bytes 16 g; rank 1's are NoPE bytes 256 + 16 g (g < 16) and the 64
+        // RoPE values (g >= 16, 32 bytes each). All loads of a chunk are in
+        // flight while the warp waits for its tile of the ring.
         const int dt = threadIdx.x - 5 * 32;  // 0 .. 255
-        const int dw = warp - 5;
         SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
         Seg sg;
-        int ic = 0, seg = 0;
+        int ic = 0;
         bool ok = true;
         while (ok && wk.next(sg)) {
             const int n = sg.lc1 - sg.lc0;
-            if (n == 0) continue;
-            // Q rows of this CTA's 64 heads, as the A operand (K-major, 128-byte swizzle)
-            if (!(ok = mbar_wait_warp(qfree, (seg & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
-            {
-                const uint4 *qsrc = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                                                                    ((size_t)sg.b * p.H_q + hh * HEADS) * DQK);
-                for (int e = dt; e < HEADS * (DQK / 8); e += DQ_WARPS * 32) {
-                    const int h = e / (DQK / 8), c = e % (DQK / 8);
-                    *reinterpret_cast<uint4 *>(smem + OFF_Q + (c >> 3) * SLICE + swz(h, c & 7)) = qsrc[e];
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qfull);
             const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
             for (int c = 0; c < n && ok; ++c) {
-                const int cur = ic + c, kb = cur & 1;
-                const int t0 = (sg.lc0 + c) * kChunk + 8 * dw;  // first of this warp's 8 tokens
-                // the 8 tokens lie in one page (page sizes are multiples of 8)
-                const uint8_t *rows = nullptr;
-                if (t0 < sg.L) {
-                    const int pg = bt_row[t0 / p.page_size];
-                    if (pg < 0 || pg >= p.num_pages) {
-                        if (lane == 0) {
+                const int cur = ic + c, kb = cur % NK;
+                const int tbase = (sg.lc0 + c) * kChunk;
+                uint4 ra[5], rb[5];
+                float sc[5];
+#pragma unroll
+                for (int i = 0; i < 5; ++i) {
+                    const int u = dt + 256 * i, tok = u / UNITS, g = u % UNITS;
+                    const int t = tbase + tok;
+                    ra[i] = make_uint4(0u, 0u, 0u, 0u);
+                    rb[i] = ra[i];
+                    sc[i] = 0.f;
+                    if (t < sg.L) {
+                        const int pg = bt_row[t / p.page_size];
+                        if (pg < 0 || pg >= p.num_pages) {
                             atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
                             p.meta.header[kHErrorDetail] = pg;
+                        } else {
+                            const uint8_t *row = p.pool + ((size_t)pg * p.page_size + t % p.page_size) * ROW_BYTES;
+                            if (rank == 1 && g >= 16) {
+                                ra[i] = ldg_stream16(row + 528 + 32 * (g - 16));
+                                rb[i] = ldg_stream16(row + 528 + 32 * (g - 16) + 16);
+                            } else {
+                                const int byte = 256 * (int)rank + 16 * g;
+                                ra[i] = ldg_stream16(row + byte);
+                                sc[i] = ldg_stream4f(row + 512 + 4 * (byte >> 7));
+                            }
                         }
-                    } else {
-                        rows = p.pool + ((size_t)pg * p.page_size + t0 % p.page_size) * ROW_BYTES;
                     }
                 }
-                const int nv = rows ? min(8, sg.L - t0) : 0;  // valid tokens of the 8
-                uint4 nope[8], rope[8];
-                float sc[8];
+                if (!(ok = mbar_wait_warp(&kempty[kb], ((cur / NK) & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
+                uint8_t *kt = smem + OFF_K + kb * KTILE;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    nope[i] = make_uint4(0u, 0u, 0u, 0u);
-                    rope[i] = nope[i];
-                    sc[i] = 0.f;
-                    if (i < nv) {
-                        const uint8_t *r = rows + i * ROW_BYTES;
-                        nope[i] = ldg_stream16(r + 16 * lane);
-                        if (lane < 8) rope[i] = ldg_stream16(r + 528 + 16 * lane);
-                        if (lane < 4) sc[i] = ldg_stream4f(r + 512 + 4 * lane);
-                    }
-                }
-                if (!(ok = mbar_wait_warp(&kempty[kb], ((cur >> 1) & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
-                uint8_t *kt = smem + (kb ? OFF_K1 : OFF_K0);
-                // lane l's 16 values go to slice l / 4, 16-byte chunks 2 (l % 4) and 2 (l % 4) + 1;
-                // half the lanes store their upper chunk first so each store touches all banks
-                const int sl = lane >> 2, cA = 2 * (lane & 3) + ((lane >> 2) & 1), cB = cA ^ 1;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int tok = 8 * dw + i;
-                    const float scale = __shfl_sync(0xffffffffu, sc[i], lane >> 3);
-                    uint4 lo, hi;
-                    dequant16(nope[i], scale, lo, hi);
-                    const bool swap = (lane >> 2) & 1;
-                    *reinterpret_cast<uint4 *>(kt + sl * SLICE + swz(tok, cA)) = swap ? hi : lo;
-                    *reinterpret_cast<uint4 *>(kt + sl * SLICE + swz(tok, cB)) = swap ? lo : hi;
-                    if (lane < 8) *reinterpret_cast<uint4 *>(kt + 8 * SLICE + swz(tok, lane)) = rope[i];
+                for (int i = 0; i < 5; ++i) {
+                    const int u = dt + 256 * i, tok = u / UNITS, g = u % UNITS;
+                    uint4 lo = ra[i], hi = rb[i];
+                    if (!(rank == 1 && g >= 16)) dequant16(ra[i], sc[i], lo, hi);
+                    // window dims 16 g .. 16 g + 15: slice g / 4, chunks 2 (g % 4) and + 1; every
+                    // other group of four units stores its upper chunk first (fewer bank conflicts)
+                    const int sl = g >> 2, c0 = 2 * (g & 3);
+                    const bool swap = (g >> 2) & 1;
+                    *reinterpret_cast<uint4 *>(kt + sl * KSLICE + swz(tok, c0 + (swap ? 1 : 0))) = swap ? hi : lo;
+                    *reinterpret_cast<uint4 *>(kt + sl * KSLICE + swz(tok, c0 + (swap ? 0 : 1))) = swap ? lo : hi;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&kfull[kb]);
             }
             ic += n;
-            ++seg;
         }
         if (!ok && lane == 0) {
             atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
             *abort_flag = 1;
         }
     } else {
-        // ------------------------------------------------------------ softmax and epilogue (warps 1-4)
-        const int quad = warp & 3;                 // TMEM lanes [32 quad, 32 quad + 32)
-        const int head = quad * 16 + lane;         // owned head (lanes 0-15)
-        const bool owner = lane < 16;
+        // ------------------------------------------------------------ Q load, softmax, epilogue (warps 1-4)
+        const int quad = warp & 3;
+        const int head = quad * 32 + lane;         // this thread's row of S, P, O and Q in tensor memory
         const int sid = threadIdx.x - 32;          // 0 .. 127
+        const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
         const float sl2 = p.scale_log2;
+        const uint32_t x_peer = mapa_shared(smem_u32(smem + OFF_X), peer);
+        const uint32_t xfull_peer = mapa_shared(smem_u32(xfull), peer);
+        const uint32_t xfree_peer = mapa_shared(smem_u32(xfree), peer);
+        const int d_base = 256 * (int)rank;        // value dims held by this CTA: [d_base, d_base + 256)
         SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
         Seg sg;
         int ic = 0, seg = 0;
         bool ok = true;
-        while (wk.next(sg)) {
+        while (ok && wk.next(sg)) {
             const int n = sg.lc1 - sg.lc0;
             const bool direct = sg.ns == 1;
             const int split = sg.so + sg.s;
             const bool split_ok = direct || (split >= 0 && split < p.meta.max_splits);
+            __nv_bfloat16 *out_row =
+                reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)sg.b * p.H_q + head) * DV + d_base;
+            float *part_row = p.meta.o_part + ((size_t)split * p.H_q + head) * DV + d_base;
             if (n == 0) {
-                // no tokens: output 0, lse -inf
-                for (int e = sid; e < HEADS * DV; e += 128) {
-                    const size_t hq = (size_t)hh * HEADS + e / DV;
+                // no tokens: output 0 for this CTA's value dims, lse -inf (rank 0)
+                for (int k = 0; k < 32; ++k) {
                     if (direct)
-                        reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sg.b * p.H_q + hq) * DV + e % DV] =
-                            __float2bfloat16_rn(0.f);
+                        reinterpret_cast<uint4 *>(out_row)[k] = make_uint4(0u, 0u, 0u, 0u);
                     else if (split_ok)
-                        p.meta.o_part[((size_t)split * p.H_q + hq) * DV + e % DV] = 0.f;
+                        reinterpret_cast<float4 *>(part_row)[2 * k] = reinterpret_cast<float4 *>(part_row)[2 * k + 1] =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                if (sid < HEADS) {
-                    const size_t hq = (size_t)hh * HEADS + sid;
+                if (rank == 0) {
                     if (direct)
-                        p.lse[(size_t)sg.b * p.H_q + hq] = -INFINITY;
+                        p.lse[(size_t)sg.b * p.H_q + head] = -INFINITY;
                     else if (split_ok)
-                        p.meta.lse_part[(size_t)split * p.H_q + hq] = -INFINITY;
+                        p.meta.lse_part[(size_t)split * p.H_q + head] = -INFINITY;
                 }
                 continue;
             }
+            // this head's q, dims [288 r, 288 r + 288), into tensor memory as the A operand of S
+            if (!(ok = mbar_wait_warp(qfree, (seg & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
+            {
+                const uint4 *qs = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                                                                 ((size_t)sg.b * HQ + head) * DQK + 288 * rank);
+#pragma unroll 1
+                for (int j = 0; j < 9; ++j) {  // 32 dims = 16 columns per store
+                    uint32_t r[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = qs[4 * j + k];
+                        r[4 * k] = v.x;
+                        r[4 * k + 1] = v.y;
+                        r[4 * k + 2] = v.z;
+                        r[4 * k + 3] = v.w;
+                    }
+                    tmem_st16(trow + Q_COL + 16 * j, r);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qfull);
             float m_used = -INFINITY, l = 0.f;
             for (int c = 0; c < n; ++c) {
-                const int cur = ic + c, sb = cur & 1;
-                bool w_ok = mbar_wait_warp(&sfull[sb], (cur >> 1) & 1, abort_flag, p.wait_limit_ns);
+                const int cur = ic + c;
+                bool w_ok = mbar_wait_warp(sfull, cur & 1, abort_flag, p.wait_limit_ns);
                 tc_fence_after();
                 float s[64];
                 {
                     uint32_t r[64];
-                    tmem_ld64_sync(tmem + ((uint32_t)(32 * quad) << 16) + S_COL + 64 * sb, r);
+                    tmem_ld64_sync(trow + S_COL, r);
 #pragma unroll
                     for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sfree[sb]);
+                if (lane == 0) mbar_arrive(sfree);
+                // swap partial rows with the peer: ours into its buffer once it has
+                // consumed the previous one, then add the peer's into ours
+                if (sid == 0) mbar_arrive_expect_tx(xfull, HQ * kChunk * 4);
+                if (cur > 0) w_ok = w_ok && mbar_wait_warp(xfree, (cur - 1) & 1, abort_flag, p.wait_limit_ns);
+                if (w_ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        st_async_v4(x_peer + xoff(head, i),
+                                    make_uint4(__float_as_uint(s[4 * i]), __float_as_uint(s[4 * i + 1]),
+                                               __float_as_uint(s[4 * i + 2]), __float_as_uint(s[4 * i + 3])),
+                                    xfull_peer);
+                }
+                w_ok = w_ok && mbar_wait_warp_cluster(xfull, cur & 1, abort_flag, p.wait_limit_ns);
+                if (w_ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_X + xoff(head, i));
+                        s[4 * i] += __uint_as_float(v.x);
+                        s[4 * i + 1] += __uint_as_float(v.y);
+                        s[4 * i + 2] += __uint_as_float(v.z);
+                        s[4 * i + 3] += __uint_as_float(v.w);
+                    }
+                    // the sums above consumed every load, so the peer may overwrite the buffer
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer);
+                }
                 const int nvalid = sg.L - (sg.lc0 + c) * kChunk;
                 float mx = -INFINITY;
 #pragma unroll
@@ -375,13 +451,9 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     s[e] = (e < nvalid) ? s[e] * sl2 : -INFINITY;
                     mx = fmaxf(mx, s[e]);
                 }
-                // P's buffer and O^T are free once the previous chunk's PV has completed
+                // P's columns and O are free once the previous chunk's PV has completed
                 if (cur > 0) w_ok = w_ok && mbar_wait_warp(pfree, (cur - 1) & 1, abort_flag, p.wait_limit_ns);
-                const float m_new = fmaxf(m_used, mx);
-                const bool need = owner && c > 0 && (m_new > m_used + RESCALE_LOG2);
-                if (c == 0) m_used = m_new;
-                // both decisions are taken by all four warps together
-                if (named_barrier_or(1, 128, !w_ok || *abort_flag != 0)) {
+                if (__any_sync(0xffffffffu, !w_ok || *abort_flag != 0)) {
                     if (lane == 0) {
                         atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
                         *abort_flag = 1;
@@ -389,35 +461,27 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     ok = false;
                     break;
                 }
-                if (named_barrier_or(1, 128, need)) {
-                    {
-                        const float alpha = need ? ex2(m_used - m_new) : 1.f;
-                        if (need) {
-                            m_used = m_new;
-                            l *= alpha;
-                        }
-                        if (owner) alpha_sm[head] = alpha;
-                        named_barrier_sync(1, 128);
-                        // rescale every O^T row this thread holds (row = d_v, column = head)
+                tc_fence_after();
+                const float m_new = fmaxf(m_used, mx);
+                const bool need = c > 0 && (m_new > m_used + RESCALE_LOG2);
+                if (c == 0) m_used = m_new;
+                if (__any_sync(0xffffffffu, need)) {
+                    // re-base: scale this head's O row (tensor-memory loads and stores are warp-wide)
+                    const float alpha = need ? ex2(m_used - m_new) : 1.f;
+                    if (need) {
+                        m_used = m_new;
+                        l *= alpha;
+                    }
 #pragma unroll 1
-                        for (int j = 0; j < 4; ++j) {
-#pragma unroll 1
-                            for (int k = 0; k < 4; ++k) {
-                                uint32_t r[16];
-                                const uint32_t ta = tmem + ((uint32_t)(32 * quad) << 16) + O_COL + 64 * j + 16 * k;
-                                tmem_ld16_sync(ta, r);
+                    for (int k = 0; k < 16; ++k) {
+                        uint32_t r[16];
+                        tmem_ld16_sync(trow + O_COL + 16 * k, r);
 #pragma unroll
-                                for (int e = 0; e < 16; ++e)
-                                    r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha_sm[16 * k + e]);
-                                tmem_st16(ta, r);
-                            }
-                        }
-                        tmem_wait_st();
-                        tc_fence_before();
-                        named_barrier_sync(1, 128);
+                        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st16(trow + O_COL + 16 * k, r);
                     }
                 }
-                // P row of this head: 64 tokens, bf16, K-major B operand with 128-byte swizzle
+                // P row of this head: 64 tokens as bf16 pairs, the A operand of O += P V
                 float ps = 0.f;
                 uint32_t pk[32];
 #pragma unroll
@@ -427,60 +491,57 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     pk[e] = pack_bf16(p0, p1);
                 }
                 l += ps;
-                if (owner) {
+                {
+                    uint32_t r0[16], r1[16];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<uint4 *>(smem + OFF_P + swz(head, k)) =
-                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int e = 0; e < 16; ++e) {
+                        r0[e] = pk[e];
+                        r1[e] = pk[16 + e];
+                    }
+                    tmem_st16(trow + P_COL, r0);
+                    tmem_st16(trow + P_COL + 16, r1);
                 }
-                fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pfull);
             }
             if (!ok) break;
-            // ---- epilogue: O = O^T / l
-            const bool o_ok = !named_barrier_or(1, 128, !mbar_wait_warp(ofull, seg & 1, abort_flag, p.wait_limit_ns));
+            // ---- epilogue: O / l for this CTA's 256 value dims of this head
+            const bool o_ok = mbar_wait_warp(ofull, seg & 1, abort_flag, p.wait_limit_ns);
             tc_fence_after();
-            if (owner) {
-                l_sm[head] = l;
-                m_sm[head] = m_used;
-            }
-            named_barrier_sync(1, 128);
             if (o_ok) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
-                    const int d = 128 * j + 32 * quad + lane;
-#pragma unroll 1
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t r[16];
-                        tmem_ld16_sync(tmem + ((uint32_t)(32 * quad) << 16) + O_COL + 64 * j + 16 * k, r);
+                for (int k = 0; k < 16; ++k) {
+                    uint32_t r[16];
+                    tmem_ld16_sync(trow + O_COL + 16 * k, r);
+                    if (direct) {
+                        uint32_t b[8];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int h = 16 * k + e;
-                            const float lh = l_sm[h];
-                            const float o = lh > 0.f ? __uint_as_float(r[e]) / lh : 0.f;
-                            const size_t hq = (size_t)hh * HEADS + h;
-                            if (direct)
-                                reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sg.b * p.H_q + hq) * DV + d] =
-                                    __float2bfloat16_rn(o);
-                            else if (split_ok)
-                                p.meta.o_part[((size_t)split * p.H_q + hq) * DV + d] = o;
-                        }
+                        for (int e = 0; e < 8; ++e)
+                            b[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+                        reinterpret_cast<uint4 *>(out_row)[2 * k] = make_uint4(b[0], b[1], b[2], b[3]);
+                        reinterpret_cast<uint4 *>(out_row)[2 * k + 1] = make_uint4(b[4], b[5], b[6], b[7]);
+                    } else if (split_ok) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            reinterpret_cast<float4 *>(part_row)[4 * k + e] =
+                                make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                            __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ofree);
-            if (owner) {
+            if (rank == 0) {
                 const float v = l > 0.f ? (m_used + log2f(l)) * kLn2Mla : -INFINITY;
-                const size_t hq = (size_t)hh * HEADS + head;
                 if (direct)
-                    p.lse[(size_t)sg.b * p.H_q + hq] = v;
+                    p.lse[(size_t)sg.b * p.H_q + head] = v;
                 else if (split_ok)
-                    p.meta.lse_part[(size_t)split * p.H_q + hq] = v;
+                    p.meta.lse_part[(size_t)split * p.H_q + head] = v;
             }
-            named_barrier_sync(1, 128);
             if (!o_ok) {
                 if (lane == 0) {
                     atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
@@ -496,10 +557,37 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    cluster_sync_all();  // the peer has finished writing into this CTA's shared memory
 }
 
 int mla_ctas_per_part() { return 2; }
 bool mla_kernel_available() { return true; }
+
+// Parts that can run at once: clusters of two CTAs, one CTA per SM.
+int mla_max_parts() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev]) return cached[dev];
+    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1024, 2);
+    cfg.blockDim = dim3(mla::THREADS);
+    cfg.dynamicSmemBytes = mla::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 2;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n;
+    return n;
+}
 
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl) {
     cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM);
@@ -509,11 +597,15 @@ cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl) {
     cfg.blockDim = dim3(mla::THREADS);
     cfg.dynamicSmemBytes = mla::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 2;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, mla_decode_kernel, p);
 }
 
