@@ -205,6 +205,23 @@ int decode_attn_fwd_static_scratch(const da_desc *desc, const void *q, const voi
 /* Static description of a return code (never NULL). */
 const char *decode_attn_strerror(int code);
 
+#ifdef DA_PAGE_TRACE
+/* Test build only (the library compiled with -DDA_PAGE_TRACE; the product
+ * build does not export it). Makes every later decode_attn_fwd record the
+ * pool rows its kernels read into `trace` (device memory, int32, caller-owned,
+ * written in place): for the GQA formats, per (part, KV head) unit, per chunk
+ * in reading order, per TMA box of min(page_size, 64) tokens, the first pool
+ * row of the box (page * page_size + offset within the page), or -2 for a box
+ * past the sequence; for the 656-byte format, per part, per chunk, per token,
+ * the token's pool row or -2. `cap` chunks are kept per unit (later ones are
+ * not recorded); the unit stride is cap * rows_per_chunk. A null `trace`
+ * stops recording. Returns DA_ERR_DIMS for cap < 1 with a non-null trace.
+ * There is no counterpart on the pages: it checks the page gather (block
+ * table -> page -> slot, XQA page section "Hopper:一次 TMA 只搬一个页") bit for
+ * bit against a reference built from the partition and the block table. */
+int decode_attn_debug_page_trace(int32_t *trace, int32_t cap);
+#endif
+
 #ifdef __cplusplus
 }
 #endif

@@ -54,14 +54,15 @@ class DecodeAttnError(RuntimeError):
     pass
 
 
-_lib = None
+_libs = {}
 
 
 def load_library(path: str = LIB_PATH):
-    """Load the shared library (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load the shared library (raises if it has not been built). Each path is
+    loaded once; the default path is the one every entry point below uses
+    unless it is given another handle (``lib=``)."""
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise DecodeAttnError(f"CUDA library not built: {path} (run paged_kv_cache_60_gb300/build.py)")
     lib = ctypes.CDLL(path)
@@ -79,7 +80,7 @@ def load_library(path: str = LIB_PATH):
     for f in ("decode_attn_sched_meta_bytes", "decode_attn_meta_offsets", "decode_attn_num_parts",
               "decode_attn_sched_meta", "decode_attn_fwd", "decode_attn_fwd_ex", "decode_attn_get_error"):
         getattr(lib, f).restype = ctypes.c_int
-    _lib = lib
+    _libs[path] = lib
     return lib
 
 
@@ -121,14 +122,14 @@ def num_parts(desc: Desc) -> int:
     return n.value
 
 
-def sched_meta(desc: Desc, cache_seqlens, meta, stream=None):
-    _check(load_library().decode_attn_sched_meta(ctypes.byref(desc), _ptr(cache_seqlens), _ptr(meta),
+def sched_meta(desc: Desc, cache_seqlens, meta, stream=None, lib=None):
+    _check((lib or load_library()).decode_attn_sched_meta(ctypes.byref(desc), _ptr(cache_seqlens), _ptr(meta),
                                                  meta.numel() * meta.element_size(), _stream(stream)))
 
 
 def fwd(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seqlens, meta, out, lse,
-        stream=None, use_pdl=True, main_begin=None, main_end=None):
-    lib = load_library()
+        stream=None, use_pdl=True, main_begin=None, main_end=None, lib=None):
+    lib = lib or load_library()
     args = (ctypes.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
             _ptr(block_table), _ptr(cache_seqlens), _ptr(meta), meta.numel() * meta.element_size(),
             _ptr(out), _ptr(lse))

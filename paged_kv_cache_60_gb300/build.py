@@ -39,10 +39,10 @@ def _headers():
     return hs
 
 
-def _compile(src, extra, verbose):
-    obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src, extra, verbose, out_dir=OUT_DIR):
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     newest_dep = max([os.path.getmtime(src)] + [os.path.getmtime(h) for h in _headers()])
-    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and not extra:
+    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and not extra and out_dir == OUT_DIR:
         return obj, ""
     cmd = [_nvcc(), "-c", src, "-o", obj] + NVCC_FLAGS + list(extra)
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -51,26 +51,31 @@ def _compile(src, extra, verbose):
     return obj, (r.stdout + r.stderr) if verbose else ""
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source and link the shared library. Returns its path."""
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), out_dir: str = OUT_DIR) -> str:
+    """Compile every CUDA source and link the shared library. Returns its path.
+
+    ``out_dir`` other than the default builds a separate copy (used for the
+    page-trace test build, ``extra_flags=("-DDA_PAGE_TRACE",)``); such a build
+    is always recompiled."""
+    os.makedirs(out_dir, exist_ok=True)
+    lib_path = os.path.join(out_dir, os.path.basename(LIB_PATH))
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra_flags, verbose), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra_flags, verbose, out_dir), srcs))
     objs = [o for o, _ in results]
     for _, log in results:
         if log:
             sys.stderr.write(log)
-    if (os.path.exists(LIB_PATH) and not extra_flags
-            and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(o) for o in objs)):
-        return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if (os.path.exists(lib_path) and not extra_flags and out_dir == OUT_DIR
+            and os.path.getmtime(lib_path) >= max(os.path.getmtime(o) for o in objs)):
+        return lib_path
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [_nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -81,6 +81,10 @@ int resolve_sms(const da_desc *d, int *nsm) {
     return DA_OK;
 }
 
+// Page-trace test build: where the kernels record the pool rows they read.
+int32_t *g_page_trace = nullptr;
+int32_t g_page_trace_cap = 0;
+
 int cpc_of(const da_desc *d) { return is_mla(d) ? mla_ctas_per_part() : 1; }
 
 int make_layout(const da_desc *d, MetaLayout *L) {
@@ -323,6 +327,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
         p.wait_limit_ns = kWaitLimitNs;
+        p.page_trace = g_page_trace;
+        p.page_trace_cap = g_page_trace_cap;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_gqa(desc->D_qk, fp8, tkv, tv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     } else {
@@ -343,6 +349,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
         p.wait_limit_ns = kWaitLimitNs;
+        p.page_trace = g_page_trace;
+        p.page_trace_cap = g_page_trace_cap;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     }
@@ -395,3 +403,18 @@ const char *decode_attn_strerror(int code) {
 }
 
 }  // extern "C"
+
+#ifdef DA_PAGE_TRACE
+// Test build only (compiled with -DDA_PAGE_TRACE): record the pool rows every
+// later decode_attn_fwd reads into `trace` (device, int32). GQA: per (part, KV
+// head) CTA, per chunk, per TMA box: the first pool row of the box (page *
+// page_size + offset in the page) or -2 for a box past the sequence. MLA: per
+// part, per chunk, per token: the token's pool row or -2. `cap` chunks are kept
+// per CTA / part. Pass null to stop recording.
+extern "C" int decode_attn_debug_page_trace(int32_t *trace, int32_t cap) {
+    if (trace && cap < 1) return DA_ERR_DIMS;
+    g_page_trace = trace;
+    g_page_trace_cap = trace ? cap : 0;
+    return DA_OK;
+}
+#endif

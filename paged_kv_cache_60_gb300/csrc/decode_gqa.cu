@@ -178,6 +178,14 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                         p.meta.header[kHErrorDetail] = pg;
                         pg = -2;  // skipped: its rows keep stale bytes
                     }
+#ifdef DA_PAGE_TRACE
+                    if (p.page_trace && i < p.page_trace_cap) {
+                        const int tok = (lc + k) * kChunk + lane * bt;
+                        const size_t unit = (size_t)blockIdx.x * gridDim.y + blockIdx.y;
+                        p.page_trace[(unit * p.page_trace_cap + i) * nb + lane] =
+                            pg == -2 ? -2 : pg * P + ((P > kChunk) ? (tok % P) : 0);
+                    }
+#endif
                     mbar_arrive_expect_tx(&full[stage], pg == -2 ? 0u : box_bytes);
                     if (pg != -2) {
                         const int tok = (lc + k) * kChunk + lane * bt;

@@ -298,6 +298,11 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     ra[i] = make_uint4(0u, 0u, 0u, 0u);
                     rb[i] = ra[i];
                     sc[i] = 0.f;
+#ifdef DA_PAGE_TRACE
+                    if (p.page_trace && rank == 0 && g == 0 && cur < p.page_trace_cap)
+                        p.page_trace[((size_t)part * p.page_trace_cap + cur) * kChunk + tok] =
+                            t < sg.L ? bt_row[t / p.page_size] * p.page_size + t % p.page_size : -2;
+#endif
                     if (t < sg.L) {
                         const int pg = bt_row[t / p.page_size];
                         if (pg < 0 || pg >= p.num_pages) {

@@ -83,6 +83,8 @@ struct GqaParams {
     int32_t splits, num_parts;
     float scale_log2;              // softmax_scale * log2(e)
     uint64_t wait_limit_ns;
+    int32_t *page_trace;           // page-trace test build only (null otherwise): rows read, per box
+    int32_t page_trace_cap;        // chunks recorded per CTA
 };
 
 struct MlaParams {
@@ -97,6 +99,8 @@ struct MlaParams {
     int32_t splits, num_parts;
     float scale_log2;
     uint64_t wait_limit_ns;
+    int32_t *page_trace;           // page-trace test build only (null otherwise): rows read, per token
+    int32_t page_trace_cap;        // chunks recorded per part
 };
 
 struct CombineParams {
