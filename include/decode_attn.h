@@ -220,6 +220,20 @@ const char *decode_attn_strerror(int code);
  * table -> page -> slot, XQA page section "Hopper:一次 TMA 只搬一个页") bit for
  * bit against a reference built from the partition and the block table. */
 int decode_attn_debug_page_trace(int32_t *trace, int32_t cap);
+
+/* Test build only. Limits every bounded wait (mbarrier phase, peer CTA) of
+ * later launches to `ns` nanoseconds; 0 restores the product limit of 2 s. A
+ * wait that runs out sets DA_DEV_TIMEOUT in the device error word, the
+ * kernel's CTAs stop their work units and return, and the CUDA context stays
+ * usable; it exists so that tests can make waits run out without a fault.
+ * No counterpart on the pages. Always returns DA_OK. */
+int decode_attn_debug_wait_limit(uint64_t ns);
+
+/* Test build only. With `on` != 0, the consumer warps of later GQA-format
+ * launches first wait (bounded, see above) on an mbarrier that nothing
+ * completes: the wait runs out, DA_DEV_TIMEOUT is set and the CTAs return.
+ * 0 turns it off. No counterpart on the pages. Always returns DA_OK. */
+int decode_attn_debug_stall(int32_t on);
 #endif
 
 #ifdef __cplusplus

@@ -81,9 +81,12 @@ int resolve_sms(const da_desc *d, int *nsm) {
     return DA_OK;
 }
 
-// Page-trace test build: where the kernels record the pool rows they read.
+// Page-trace test build: where the kernels record the pool rows they read,
+// and an optional shorter limit for every bounded wait.
 int32_t *g_page_trace = nullptr;
 int32_t g_page_trace_cap = 0;
+uint64_t g_wait_limit_ns = 0;  // 0: kWaitLimitNs
+int32_t g_debug_stall = 0;
 
 int cpc_of(const da_desc *d) { return is_mla(d) ? mla_ctas_per_part() : 1; }
 
@@ -326,9 +329,10 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.splits = desc->splits;
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
-        p.wait_limit_ns = kWaitLimitNs;
+        p.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitLimitNs;
         p.page_trace = g_page_trace;
         p.page_trace_cap = g_page_trace_cap;
+        p.debug_stall = g_debug_stall;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_gqa(desc->D_qk, fp8, tkv, tv, p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     } else {
@@ -348,7 +352,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.splits = desc->splits;
         p.num_parts = L.num_parts;
         p.scale_log2 = sigma * kLog2eF;
-        p.wait_limit_ns = kWaitLimitNs;
+        p.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitLimitNs;
         p.page_trace = g_page_trace;
         p.page_trace_cap = g_page_trace_cap;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
@@ -415,6 +419,20 @@ extern "C" int decode_attn_debug_page_trace(int32_t *trace, int32_t cap) {
     if (trace && cap < 1) return DA_ERR_DIMS;
     g_page_trace = trace;
     g_page_trace_cap = trace ? cap : 0;
+    return DA_OK;
+}
+
+// Test build only: limit every bounded wait of later launches to `ns`
+// nanoseconds (0 restores the default of 2 s).
+extern "C" int decode_attn_debug_wait_limit(uint64_t ns) {
+    g_wait_limit_ns = ns;
+    return DA_OK;
+}
+
+// Test build only: with `on` != 0, the GQA kernel's consumer warps first wait
+// on a barrier that nothing completes, so that wait runs out.
+extern "C" int decode_attn_debug_stall(int32_t on) {
+    g_debug_stall = on;
     return DA_OK;
 }
 #endif

@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
             mbar_init(&empty[i], 1);
         }
         *abort_flag = 0;
+#ifdef DA_PAGE_TRACE
+        mbar_init(reinterpret_cast<uint64_t *>(smem + C::OFF_FLAG + 8), 1);  // never arrived at
+#endif
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -203,9 +206,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
             }
         }
         if (aborted) {
-            // let copies already in flight land before the CTA exits
-            for (int k = max(0, i - C::NS); k < i; ++k)
-                mbar_wait_bounded(&full[k % C::NS], (k / C::NS) & 1, abort_flag, 100000000ull);
+            // let copies already in flight land before the CTA exits (ignoring the abort flag)
+            for (int k = max(0, i - C::NS); k < i; ++k) mbar_wait_timed(&full[k % C::NS], (k / C::NS) & 1, 100000000ull);
         }
         return;
     }
@@ -278,6 +280,17 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         for (int lc = lc0; lc < lc1; ++lc, ++i) {
             if ((i % C::NCW) != warp) continue;  // one warp per chunk, round robin
             const int stage = i % C::NS;
+#ifdef DA_PAGE_TRACE
+            // test build: a wait on a barrier that nothing completes runs out
+            if (p.debug_stall &&
+                !mbar_wait_warp(reinterpret_cast<uint64_t *>(smem + C::OFF_FLAG + 8), 0, abort_flag, p.wait_limit_ns)) {
+                if (lane == 0) {
+                    atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+#endif
             if (!mbar_wait_warp(&full[stage], (i / C::NS) & 1, abort_flag, p.wait_limit_ns)) {
                 if (lane == 0) {
                     atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);

@@ -85,6 +85,7 @@ struct GqaParams {
     uint64_t wait_limit_ns;
     int32_t *page_trace;           // page-trace test build only (null otherwise): rows read, per box
     int32_t page_trace_cap;        // chunks recorded per CTA
+    int32_t debug_stall;           // test build only: consumers first wait on a barrier nothing completes
 };
 
 struct MlaParams {

@@ -1,5 +1,8 @@
 """Helpers for the GPU tests: move a workload to the device, call the library
 through its C ABI binding, read back the scheduling metadata."""
+import ctypes
+import os
+
 import torch
 
 import paged_kv_cache_60_gb300 as da
@@ -12,6 +15,29 @@ LSE_TOL = 1e-4      # max |lse - oracle|
 def ensure_built():
     dabuild.build()
     return da.load_library()
+
+
+TRACE_DIR = os.path.join(os.path.dirname(os.path.dirname(dabuild.LIB_PATH)), "_build_trace")
+_trace_lib = None
+
+
+def debug_build_library():
+    """The library compiled with -DDA_PAGE_TRACE into its own directory (built
+    once per process): it adds decode_attn_debug_page_trace,
+    decode_attn_debug_wait_limit and decode_attn_debug_stall to the product
+    entry points."""
+    global _trace_lib
+    if _trace_lib is None:
+        path = dabuild.build(extra_flags=("-DDA_PAGE_TRACE",), out_dir=TRACE_DIR)
+        lib = da.load_library(path)
+        lib.decode_attn_debug_page_trace.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+        lib.decode_attn_debug_page_trace.restype = ctypes.c_int
+        lib.decode_attn_debug_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.decode_attn_debug_wait_limit.restype = ctypes.c_int
+        lib.decode_attn_debug_stall.argtypes = [ctypes.c_int32]
+        lib.decode_attn_debug_stall.restype = ctypes.c_int
+        _trace_lib = lib
+    return _trace_lib
 
 
 def device_sms() -> int:

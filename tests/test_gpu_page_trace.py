@@ -5,21 +5,18 @@ oracle's partition and the block table: for each work unit (part, KV head),
 chunk by chunk, the rows its boxes (GQA: one TMA box of min(P, 64) tokens;
 MLA: one token) must read, and -2 where a box lies past the sequence."""
 import ctypes
-import os
 
 import pytest
 import torch
 
 import paged_kv_cache_60_gb300 as da
 from oracle.sched_ref import CHUNK, part_segments, sched_ref
-from paged_kv_cache_60_gb300 import build as dabuild
 from workloads import KV_BF16, KV_FP8, KV_MLA656, WorkloadSpec, make_workload
 
-from gpu_util import DeviceWorkload, device_sms, make_desc
+from gpu_util import DeviceWorkload, device_sms, make_desc, debug_build_library
 
 pytestmark = pytest.mark.gpu
 
-TRACE_DIR = os.path.join(os.path.dirname(os.path.dirname(dabuild.LIB_PATH)), "_build_trace")
 FILL = -7
 
 
@@ -27,11 +24,7 @@ FILL = -7
 def tlib():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
-    path = dabuild.build(extra_flags=("-DDA_PAGE_TRACE",), out_dir=TRACE_DIR)
-    lib = da.load_library(path)
-    lib.decode_attn_debug_page_trace.argtypes = [ctypes.c_void_p, ctypes.c_int32]
-    lib.decode_attn_debug_page_trace.restype = ctypes.c_int
-    return lib
+    return debug_build_library()
 
 
 def _reference(w, ref, rows_per_chunk, row_of):
