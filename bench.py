@@ -186,10 +186,16 @@ class DevCopy:
         self.out = torch.empty(s.B, s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(s.B, s.H_q, dtype=torch.float32, device=dev)
 
-    def step(self, da, desc, stream, **kw):
+    def sched(self, da, desc, stream):
         da.sched_meta(desc, self.cache_seqlens, self.meta, stream=stream)
+
+    def fwd(self, da, desc, stream, **kw):
         da.fwd(desc, self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale, self.block_table,
                self.cache_seqlens, self.meta, self.out, self.lse, stream=stream, **kw)
+
+    def step(self, da, desc, stream, **kw):
+        self.sched(da, desc, stream)
+        self.fwd(da, desc, stream, **kw)
 
 
 def oracle_time_per_call(w, budget_s):
@@ -274,45 +280,82 @@ def run_ours(args, rank, world, local):
     devs = [DevCopy(torch, w, desc, da) for _ in range(copies)]
     stream = torch.cuda.Stream()
     steps, warm = args.steps, max(3, args.warmup)
-    launches_per_step = 3
+    # A call is decode_attn_fwd (split-KV kernel + combine) on scheduling
+    # metadata built once beforehand and reused, as every layer of a decode
+    # step reuses it; decode_attn_sched_meta is timed on its own and together
+    # with the call (sched_meta_us, with_sched_meta_us).
+    launches_per_step = 2
 
-    # ---- graphs (one per input copy), or eager
-    graphs = None
+    # ---- CUDA graphs of several calls each (calls rotate over the input
+    # copies, so consecutive calls read different memory), or eager launches.
+    # A graph holds cpg calls; n calls replay it n // cpg times plus a graph of
+    # the remaining n % cpg calls, so exactly n calls run.
+    cpg = copies * max(1, -(-8 // copies))
+    fns = {"fwd": lambda d: d.fwd(da, desc, stream), "both": lambda d: d.step(da, desc, stream),
+           "sched": lambda d: d.sched(da, desc, stream)}
+    graph_cache = {}
     with torch.cuda.stream(stream):
         for d in devs:
             d.step(da, desc, stream)
         torch.cuda.synchronize()
-        if not args.eager:
-            graphs = []
-            for d in devs:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    d.step(da, desc, stream)
-                graphs.append(g)
-        torch.cuda.synchronize()
 
-    def do_step(k):
-        if graphs is not None:
-            graphs[k % copies].replay()
-        else:
-            devs[k % copies].step(da, desc, stream)
+    def graph_of(which, ncalls):
+        key = (which, ncalls)
+        if key not in graph_cache:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    for j in range(ncalls):
+                        fns[which](devs[j % copies])
+            torch.cuda.synchronize()
+            graph_cache[key] = g
+        return graph_cache[key]
+
+    def run_calls(n, which="fwd"):
+        if args.eager:
+            for k in range(n):
+                fns[which](devs[k % copies])
+            return
+        for _ in range(n // cpg):
+            graph_of(which, cpg).replay()
+        if n % cpg:
+            graph_of(which, n % cpg).replay()
+
+    def timed(which, n):
+        if not args.eager:  # capture before timing
+            graph_of(which, cpg)
+            if n % cpg:
+                graph_of(which, n % cpg)
+        with torch.cuda.stream(stream):
+            run_calls(min(n, 3 * cpg), which)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run_calls(n, which)
+            b.record(stream)
+            torch.cuda.synchronize()
+        return a.elapsed_time(b) / n * 1000.0
 
     bus = torch.cuda.get_device_properties(local)
     bus_id = getattr(bus, "pci_bus_id", None)
     bus_str = f"{getattr(bus, 'pci_domain_id', 0):08x}:{bus_id:02x}:{getattr(bus, 'pci_device_id', 0):02x}.0" \
         if isinstance(bus_id, int) else ""
 
+    if not args.eager:
+        graph_of("fwd", cpg)
+        if steps % cpg:
+            graph_of("fwd", steps % cpg)
+        if warm % cpg:
+            graph_of("fwd", warm % cpg)
     with torch.cuda.stream(stream):
-        for k in range(warm):
-            do_step(k)
+        run_calls(warm)
         torch.cuda.synchronize()
         dist_barrier(world)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(bus_str) as clk:
             e0.record(stream)
-            for k in range(steps):
-                do_step(k)
+            run_calls(steps)
             e1.record(stream)
             torch.cuda.synchronize()
         dist_barrier(world)
@@ -331,9 +374,12 @@ def run_ours(args, rank, world, local):
             b.record(stream)
         torch.cuda.synchronize()
         for k, (a, b) in enumerate(evs):
-            devs[k % copies].step(da, desc, stream, main_begin=a, main_end=b)
+            devs[k % copies].fwd(da, desc, stream, main_begin=a, main_end=b)
         torch.cuda.synchronize()
     main_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    n_side = max(3, min(steps, 200))
+    sched_us = timed("sched", n_side)
+    both_us = timed("both", n_side)
     hbm_peak, tc_peak, peak_kind = load_peaks()
     key = "mla" if spec.kv_dtype == da.KV_MLA656 else "gqa"
     traffic = profile_traffic(key, args.workload)
@@ -383,6 +429,7 @@ def run_ours(args, rank, world, local):
         e2e_us = a.elapsed_time(b) / n_e2e * 1000.0
         e2e_us = dist_max(e2e_us, world) / world
         e2e = {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+               "includes": "pinned host inputs to device, decode_attn_sched_meta, decode_attn_fwd, out and lse to host",
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     cpu = None
@@ -404,9 +451,13 @@ def run_ours(args, rank, world, local):
                        "splits": spec.splits, "kv_bytes_per_call": kv_bytes,
                        "l2": ("inputs rotate over %d copies (%.0f MB > 2x L2)" % (copies, copies * kv_bytes / 1e6))
                        if copies > 1 else "inputs larger than 2x L2",
-                       "launch": "eager" if args.eager else "cuda graph per step",
+                       "launch": "eager" if args.eager else f"cuda graphs of {cpg} calls",
+                       "call": "decode_attn_fwd (split-KV kernel + PDL-chained combine) on scheduling "
+                               "metadata built once and reused; decode_attn_sched_meta timed separately",
                        "parallelism": f"replicas x{world}"},
             "kv_read_gbs": round(kv_bytes / (ms * 1e-3) / 1e9 * world, 1),
+            "sched_meta_us": round(sched_us, 3),
+            "with_sched_meta_us": round(both_us, 3),
             "roofline": roofline,
             "clocks": clk.summary(),
             "gpu_launches": launches_per_step * steps,
