@@ -57,8 +57,9 @@ def dist_init(n):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl" if n > 0 else "gloo"
+        backend = "nccl" if n > 0 and torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
     return rank, world, local
 
@@ -68,7 +69,7 @@ def dist_max(x, world):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
