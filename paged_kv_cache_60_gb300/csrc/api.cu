@@ -124,6 +124,8 @@ int make_layout(const da_desc *d, MetaLayout *L) {
     off += round_up((size_t)max_splits * H_q * 4, 256);
     L->o_part = off;
     off += round_up((size_t)max_splits * H_q * d->D_v * 4, 256);
+    L->xchg = off;  // per part, per CTA of the pair: 128 heads x 64 tokens fp32
+    if (is_mla(d)) off += round_up((size_t)num_parts * 2 * H_q * kChunk * 4, 256);
     L->total = off;
     L->num_parts = (int32_t)num_parts;
     L->max_splits = (int32_t)max_splits;
@@ -141,6 +143,7 @@ MetaView meta_view(void *meta, const MetaLayout &L) {
     v.num_splits = reinterpret_cast<const int32_t *>(base + L.num_splits);
     v.lse_part = reinterpret_cast<float *>(base + L.lse_part);
     v.o_part = reinterpret_cast<float *>(base + L.o_part);
+    v.xchg = reinterpret_cast<float *>(base + L.xchg);
     v.max_splits = L.max_splits;
     return v;
 }

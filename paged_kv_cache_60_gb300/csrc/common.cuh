@@ -321,6 +321,8 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, const uint4 &v, uint
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 // Every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");

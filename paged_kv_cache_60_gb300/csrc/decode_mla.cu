@@ -14,9 +14,10 @@
 // [256 r, 256 r + 320) of each latent row:
 //   S_r = Q[:, 288 r : 288 r + 288] K[:, same]^T   M = 128 heads, N = 64 tokens, 18 MMAs,
 //                                                 Q read from tensor memory
-//   the two partial S are swapped through distributed shared memory and added
-//   (fp32 addition commutes, so both CTAs hold the same S bit for bit and take
-//   the same softmax decisions without further exchange);
+//   the two partial S are swapped through L2 (a slot per CTA in the
+//   scheduling-metadata buffer, signalled through the cluster's mbarriers) and
+//   added (fp32 addition commutes, so both CTAs hold the same S bit for bit and
+//   take the same softmax decisions without further exchange);
 //   O[:, 256 r : 256 r + 256] += P V               M = 128 heads, N = 256 dims, 4 MMAs,
 //                                                 P read from tensor memory
 // So each CTA dequantises 320 of the 576 values of a token, and O (128 heads x
@@ -51,10 +52,8 @@ constexpr int KSLICE = kChunk * 128;       // one slice of a 64-token tile (8 KB
 constexpr int KTILE = WSL * KSLICE;        // 40 KB
 constexpr int NK = 4;                      // depth of the dequantised-tile ring
 constexpr int ROW_BYTES = 656;
-constexpr int XROW = kChunk * 4 + 16;      // exchange-buffer row: 64 fp32 + 16 bytes of padding
 constexpr int OFF_K = 0;                   // NK tiles
-constexpr int OFF_X = NK * KTILE;          // the peer's partial S: 128 heads x 64 tokens fp32
-constexpr int OFF_MISC = OFF_X + HQ * XROW;
+constexpr int OFF_MISC = NK * KTILE;
 // misc: mbarriers, tmem base, abort flag
 constexpr int NBARS = 2 * NK + 10;
 constexpr int OFF_BARS = OFF_MISC;
@@ -115,10 +114,6 @@ __device__ __forceinline__ void dequant16(const uint4 v, float scale, uint4 &lo,
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// Position of 16-byte chunk i of head h's 256-byte row in the exchange buffer:
-// rows are padded to 272 bytes, so a warp's stores and loads spread over all
-// banks while the chunk offsets stay constants.
-__device__ __forceinline__ uint32_t xoff(int h, int i) { return (uint32_t)(h * mla::XROW + 16 * i); }
 
 __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __grid_constant__ MlaParams p) {
     using namespace mla;
@@ -151,7 +146,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         mbar_init(ofree, SM_THREADS / 32);
         mbar_init(qfull, SM_THREADS / 32);
         mbar_init(qfree, 1);
-        mbar_init(xfull, 1);  // armed locally; the peer's stores count their bytes
+        mbar_init(xfull, SM_THREADS / 32);  // the peer's four softmax warps
         mbar_init(xfree, SM_THREADS / 32);
         *abort_flag = 0;
         fence_barrier_init();
@@ -352,7 +347,10 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         const int sid = threadIdx.x - 32;          // 0 .. 127
         const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
         const float sl2 = p.scale_log2;
-        const uint32_t x_peer = mapa_shared(smem_u32(smem + OFF_X), peer);
+        // partial scores travel through L2: this CTA's slot and the peer's, laid out
+        // [16-byte column i][head] so that a warp's stores and loads are coalesced
+        float4 *x_mine = reinterpret_cast<float4 *>(p.meta.xchg) + ((size_t)part * 2 + rank) * 16 * HQ + head;
+        const float4 *x_other = reinterpret_cast<const float4 *>(p.meta.xchg) + ((size_t)part * 2 + peer) * 16 * HQ + head;
         const uint32_t xfull_peer = mapa_shared(smem_u32(xfull), peer);
         const uint32_t xfree_peer = mapa_shared(smem_u32(xfree), peer);
         const int d_base = 256 * (int)rank;        // value dims held by this CTA: [d_base, d_base + 256)
@@ -425,25 +423,24 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 if (lane == 0) mbar_arrive(sfree);
                 // swap partial rows with the peer: ours into its buffer once it has
                 // consumed the previous one, then add the peer's into ours
-                if (sid == 0) mbar_arrive_expect_tx(xfull, HQ * kChunk * 4);
                 if (cur > 0) w_ok = w_ok && mbar_wait_warp(xfree, (cur - 1) & 1, abort_flag, p.wait_limit_ns);
                 if (w_ok) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        st_async_v4(x_peer + xoff(head, i),
-                                    make_uint4(__float_as_uint(s[4 * i]), __float_as_uint(s[4 * i + 1]),
-                                               __float_as_uint(s[4 * i + 2]), __float_as_uint(s[4 * i + 3])),
-                                    xfull_peer);
+                        x_mine[i * HQ] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+                    fence_acq_rel_cluster();  // each lane's stores, before the warp's release below
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(xfull_peer);
                 }
                 w_ok = w_ok && mbar_wait_warp_cluster(xfull, cur & 1, abort_flag, p.wait_limit_ns);
                 if (w_ok) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_X + xoff(head, i));
-                        s[4 * i] += __uint_as_float(v.x);
-                        s[4 * i + 1] += __uint_as_float(v.y);
-                        s[4 * i + 2] += __uint_as_float(v.z);
-                        s[4 * i + 3] += __uint_as_float(v.w);
+                        const float4 v = __ldcg(x_other + i * HQ);
+                        s[4 * i] += v.x;
+                        s[4 * i + 1] += v.y;
+                        s[4 * i + 2] += v.z;
+                        s[4 * i + 3] += v.w;
                     }
                     // the sums above consumed every load, so the peer may overwrite the buffer
                     __syncwarp();

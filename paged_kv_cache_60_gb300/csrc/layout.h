@@ -41,7 +41,7 @@ struct PartRec {
 constexpr int kPartRecInts = 8;
 
 struct MetaLayout {
-    size_t header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part, total;
+    size_t header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part, xchg, total;
     int32_t num_parts, max_splits, cpc;
 };
 
@@ -54,6 +54,7 @@ struct MetaView {
     const int32_t *num_splits;
     float *lse_part;   // [max_splits][H_q]
     float *o_part;     // [max_splits][H_q][D_v]
+    float *xchg;       // latent-token kernel only: partial scores swapped between the CTAs of a part
     int32_t max_splits;
 };
 
