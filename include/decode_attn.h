@@ -100,7 +100,9 @@ typedef struct {
  * Size in bytes of the sched_meta buffer for this desc (host only, no CUDA
  * call except an SM-count query when desc->num_sms is 0). The buffer holds the
  * scheduling metadata, the split-KV partials (fp32 o and lse per split and
- * query head) and the device error word.
+ * query head), the device error word and, for DA_KV_FP8_MLA656, the slots in
+ * which the two CTAs of a part swap their partial scores (32 KB per CTA;
+ * rewritten by every decode_attn_fwd, never read across calls).
  */
 int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
 
