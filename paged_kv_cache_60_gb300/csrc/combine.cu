@@ -20,6 +20,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int DV>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
     pdl_wait();
+    pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid before reading
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.y * 4 + warp;
