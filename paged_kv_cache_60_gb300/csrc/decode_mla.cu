@@ -35,6 +35,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "decode_attn.h"
 #include "segwalk.cuh"
@@ -567,10 +569,10 @@ bool mla_kernel_available() { return true; }
 
 // Parts that can run at once: clusters of two CTAs, one CTA per SM.
 int mla_max_parts() {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev]) return cached[dev];
+    if (const int c = cached[dev].load(std::memory_order_relaxed)) return c;
     if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM) !=
         cudaSuccess)
         return 0;
@@ -587,7 +589,7 @@ int mla_max_parts() {
     cfg.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
