@@ -7,8 +7,11 @@ benchmark's CPU-baseline leg may import this package; the library under
 * ``decode_ref.c``  -- attention by its definition, per (request, KV head,
   head range, token range), plus the split merge; built with gcc + OpenMP.
 * ``sched_ref.py``  -- the integer split-KV scheduling metadata.
+* ``append_ref.py`` -- appending one new token per request into its page slot,
+  with the e4m3 encoder (per-head scales, or the 656-byte latent token).
 
-Parity pins for both are in tests/test_oracle.py and tests/test_sched_oracle.py.
+Parity pins are in tests/test_oracle.py, tests/test_sched_oracle.py and
+tests/test_oracle_append.py.
 """
 import ctypes
 import os
