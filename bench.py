@@ -186,6 +186,16 @@ class DevCopy:
         self.meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device=dev)
         self.out = torch.empty(s.B, s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(s.B, s.H_q, dtype=torch.float32, device=dev)
+        # one new token per request, written at its last position (decode_attn_append_kv)
+        from workloads import make_append_batch
+        k_new, v_new, pos = make_append_batch(w, seed=s.seed + 1)
+        self.k_new = k_new.to(dev)
+        self.v_new = v_new.to(dev) if v_new is not None else None
+        self.positions = pos.to(dev)
+
+    def append(self, da, desc, stream):
+        da.append_kv(desc, self.k_new, self.v_new, self.positions, self.block_table, self.k_pool, self.v_pool,
+                     self.k_scale, self.v_scale, stream=stream)
 
     def sched(self, da, desc, stream):
         da.sched_meta(desc, self.cache_seqlens, self.meta, stream=stream)
@@ -293,7 +303,8 @@ def run_ours(args, rank, world, local):
     # the remaining n % cpg calls, so exactly n calls run.
     cpg = copies * max(1, -(-8 // copies))
     fns = {"fwd": lambda d: d.fwd(da, desc, stream), "both": lambda d: d.step(da, desc, stream),
-           "sched": lambda d: d.sched(da, desc, stream)}
+           "sched": lambda d: d.sched(da, desc, stream), "append": lambda d: d.append(da, desc, stream),
+           "append_fwd": lambda d: (d.append(da, desc, stream), d.fwd(da, desc, stream))}
     graph_cache = {}
     with torch.cuda.stream(stream):
         for d in devs:
@@ -381,6 +392,18 @@ def run_ours(args, rank, world, local):
     n_side = max(3, min(steps, 200))
     sched_us = timed("sched", n_side)
     both_us = timed("both", n_side)
+    append_us = timed("append", n_side)
+    append_fwd_us = timed("append_fwd", n_side)
+    n_app = sum(1 for L in w.lengths if L > 0)
+    if spec.kv_dtype == da.KV_MLA656:
+        app_bytes = n_app * (2 * (spec.D_qk) + 656) + 8 * spec.B
+    else:
+        es = 1 if spec.kv_dtype == da.KV_FP8 else 2
+        app_bytes = n_app * 2 * spec.H_kv * spec.D_qk * (2 + es) + 8 * spec.B
+    append = {"us_per_call": round(append_us, 3), "algorithmic_bytes": app_bytes,
+              "gbs": round(app_bytes / (append_us * 1e-6) / 1e9, 1), "with_fwd_us": round(append_fwd_us, 3),
+              "call": "decode_attn_append_kv: one new token per request into its page slot "
+                      "(bf16 rows in, pool format out), then optionally decode_attn_fwd"}
     hbm_peak, tc_peak, peak_kind = load_peaks()
     key = "mla" if spec.kv_dtype == da.KV_MLA656 else "gqa"
     traffic = profile_traffic(key, args.workload)
@@ -459,6 +482,7 @@ def run_ours(args, rank, world, local):
             "kv_read_gbs": round(kv_bytes / (ms * 1e-3) / 1e9 * world, 1),
             "sched_meta_us": round(sched_us, 3),
             "with_sched_meta_us": round(both_us, 3),
+            "append": append,
             "roofline": roofline,
             "clocks": clk.summary(),
             "gpu_launches": launches_per_step * steps,

@@ -171,6 +171,48 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
                        void *out, float *lse, const da_launch_opts *opts, cudaStream_t stream);
 
 /*
+ * KV append: writes each request's new token into the pool, the step that
+ * precedes decode attention (XQA page, section "一次 decode step 的完整时序":
+ * the new K/V lands in the paged pool upstream, and the attention kernel then
+ * reads it through the page table). Request b's token, at position
+ * t = positions[b] (its index in the request: the cache_seqlens[b] of the
+ * step before, so the next decode uses t + 1), goes to slot t % page_size of
+ * page block_table[b][t / page_size], for every KV head.
+ *   desc: B, H_kv, D_qk, D_v, page_size, max_pages_per_seq, num_pages and
+ *     kv_dtype are used (the others are ignored). bf16 and e4m3 pools need
+ *     D_qk == D_v, a multiple of 8; the 656-byte token H_kv = 1, D_qk = 576,
+ *     D_v = 512. The pools are those of decode_attn_fwd.
+ *   k_new, v_new: device bf16, request b's row at (k_new + b * new_row_stride):
+ *     H_kv x D values (head-major), or for the 656-byte token the 576 values of
+ *     the latent vector (512 NoPE, then 64 RoPE) with v_new = NULL (V is the
+ *     first 512 of them). new_row_stride counts bf16 elements (0: packed rows;
+ *     else at least the row length and a multiple of 8), so rows may sit inside
+ *     a larger fused projection output.
+ *   positions: device int32 [B]; a negative position skips the request.
+ *   block_table: device int32 [B][max_pages_per_seq].
+ *   k_pool, v_pool: device, written in place; only the addressed slots change.
+ *     v_pool must be NULL or k_pool for the 656-byte token.
+ *   k_scale, v_scale: device fp32 [H_kv] for DA_KV_FP8_PER_TENSOR (read only).
+ *   device_error: device int32 or NULL; DA_DEV_SEQ_TOO_LONG (t >=
+ *     max_pages_per_seq * page_size) and DA_DEV_BAD_PAGE (page id outside
+ *     [0, num_pages)) are OR-ed into it, and such a request is skipped.
+ * Quantisation (e4m3, OCP FP8: largest finite 448): code = nearest e4m3 to the
+ * fp32 quotient x / scale (IEEE division, round to nearest even), ties to the
+ * even code, saturating at +-448, NaN -> 0x7F. Per-tensor pools divide by
+ * k_scale[h] / v_scale[h] (XQA page, section "Hopper 路径上 V 不做显式反量化");
+ * the 656-byte token (FlashMLA page, section "数据加载") takes, per block of 128
+ * NoPE values, scale = max|x| / 448 in fp32 (1 for an all-zero block), stores
+ * the 512 codes, the 4 fp32 scales and the 64 RoPE values unchanged.
+ * Pointers to bf16 rows and pools must be 16-byte aligned, the others 4-byte.
+ * Launches one kernel on `stream` (programmatic dependent launch: a following
+ * decode_attn_fwd may start early and waits for it before reading the pool).
+ * Two requests that address the same slot race. No allocation, no sync.
+ */
+int decode_attn_append_kv(const da_desc *desc, const void *k_new, const void *v_new, int64_t new_row_stride,
+                          const int32_t *positions, const int32_t *block_table, void *k_pool, void *v_pool,
+                          const float *k_scale, const float *v_scale, int32_t *device_error, cudaStream_t stream);
+
+/*
  * Reads the device error word of sched_meta into *device_error (host int32).
  * Synchronises `stream`.
  */

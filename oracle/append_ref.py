@@ -62,7 +62,9 @@ def mla_row(x_bits: np.ndarray) -> np.ndarray:
         amax = np.float32(np.max(np.abs(x[blk])))
         scale = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
         scales[blk] = scale
-        row[128 * blk:128 * blk + 128] = e4m3_encode(x[blk] / scale)
+        with np.errstate(invalid="ignore", divide="ignore", over="ignore"):   # inf / inf -> NaN -> 0x7F
+            q = x[blk] / scale
+        row[128 * blk:128 * blk + 128] = e4m3_encode(q)
     row[512:528] = scales.view(np.uint8)
     row[528:656] = x_bits[512:576].astype(np.uint16).view(np.uint8)
     return row
@@ -109,6 +111,9 @@ def append_ref(kv_dtype, page_size, k_pool, v_pool, k_new, v_new, positions, blo
                 vp[off:off + 2 * D] = vb[b, h].view(np.uint8)
             else:
                 off = ((page * P + slot) * H_kv + h) * D
-                kp[off:off + D] = e4m3_encode(_bf16_to_f32(kb[b, h]) / ks[h])
-                vp[off:off + D] = e4m3_encode(_bf16_to_f32(vb[b, h]) / vs[h])
+                with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+                    qk = _bf16_to_f32(kb[b, h]) / ks[h]
+                    qv = _bf16_to_f32(vb[b, h]) / vs[h]
+                kp[off:off + D] = e4m3_encode(qk)
+                vp[off:off + D] = e4m3_encode(qv)
     return kp, vp, err

@@ -75,10 +75,12 @@ def load_library(path: str = LIB_PATH):
     lib.decode_attn_fwd.argtypes = [DP, P, P, P, P, P, P, P, P, SZ, P, P, P]
     lib.decode_attn_fwd_ex.argtypes = [DP, P, P, P, P, P, P, P, P, SZ, P, P, ctypes.POINTER(LaunchOpts), P]
     lib.decode_attn_get_error.argtypes = [P, ctypes.POINTER(I32), P]
+    lib.decode_attn_append_kv.argtypes = [DP, P, P, ctypes.c_int64, P, P, P, P, P, P, P, P]
     lib.decode_attn_strerror.argtypes = [ctypes.c_int]
     lib.decode_attn_strerror.restype = ctypes.c_char_p
     for f in ("decode_attn_sched_meta_bytes", "decode_attn_meta_offsets", "decode_attn_num_parts",
-              "decode_attn_sched_meta", "decode_attn_fwd", "decode_attn_fwd_ex", "decode_attn_get_error"):
+              "decode_attn_sched_meta", "decode_attn_fwd", "decode_attn_fwd_ex", "decode_attn_get_error",
+              "decode_attn_append_kv"):
         getattr(lib, f).restype = ctypes.c_int
     _libs[path] = lib
     return lib
@@ -162,6 +164,18 @@ def fwd_static_scratch(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_ta
              _ptr(block_table), _ptr(cache_seqlens), _ptr(out), _ptr(lse), _stream(stream)))
 
 
+def append_kv(desc: Desc, k_new, v_new, positions, block_table, k_pool, v_pool, k_scale=None, v_scale=None,
+              device_error=None, new_row_stride=0, stream=None, lib=None):
+    """Write each request's new token (bf16 rows of k_new / v_new, v_new None
+    for the 656-byte token) into slot positions[b] % page_size of page
+    block_table[b][positions[b] // page_size], quantising for e4m3 pools;
+    see decode_attn_append_kv in the header. ``device_error``: optional
+    device int32 tensor that receives the error bits."""
+    _check((lib or load_library()).decode_attn_append_kv(
+        ctypes.byref(desc), _ptr(k_new), _ptr(v_new), int(new_row_stride), _ptr(positions), _ptr(block_table),
+        _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(device_error), _stream(stream)))
+
+
 def get_error(meta, stream=None) -> int:
     e = ctypes.c_int32(0)
     _check(load_library().decode_attn_get_error(_ptr(meta), ctypes.byref(e), _stream(stream)))
@@ -169,4 +183,4 @@ def get_error(meta, stream=None) -> int:
 
 
 __all__ = ["Desc", "LaunchOpts", "DecodeAttnError", "load_library", "strerror", "sched_meta_bytes",
-           "meta_offsets", "num_parts", "sched_meta", "fwd", "fwd_static_scratch", "get_error", "KV_BF16", "KV_FP8", "KV_MLA656"]
+           "meta_offsets", "num_parts", "sched_meta", "fwd", "fwd_static_scratch", "append_kv", "get_error", "KV_BF16", "KV_FP8", "KV_MLA656"]

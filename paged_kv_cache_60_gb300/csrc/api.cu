@@ -16,6 +16,7 @@ cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMa
                        cudaStream_t stream, bool pdl);
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl);
+cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stream, bool pdl);
 int mla_ctas_per_part();
 bool mla_kernel_available();
 int mla_max_parts();
@@ -383,6 +384,71 @@ int decode_attn_fwd(const da_desc *desc, const void *q, const void *k_pool, cons
                     cudaStream_t stream) {
     return decode_attn_fwd_ex(desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seqlens, sched_meta,
                               sched_meta_bytes, out, lse, nullptr, stream);
+}
+
+int decode_attn_append_kv(const da_desc *desc, const void *k_new, const void *v_new, int64_t new_row_stride,
+                          const int32_t *positions, const int32_t *block_table, void *k_pool, void *v_pool,
+                          const float *k_scale, const float *v_scale, int32_t *device_error, cudaStream_t stream) {
+    if (!desc) return DA_ERR_NULL;
+    const da_desc *d = desc;
+    if (d->B < 1 || d->B > (1 << 24) || d->H_kv < 1 || d->H_kv > 4096 || d->page_size < 1 ||
+        d->max_pages_per_seq < 1 || d->num_pages < 1 || d->D_qk < 1 || d->D_v < 1)
+        return DA_ERR_DIMS;
+    if ((int64_t)d->max_pages_per_seq * d->page_size > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+    if ((int64_t)d->B * d->max_pages_per_seq > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+    const bool mla = is_mla(d);
+    int64_t row_len = 0;  // bf16 values of one request's new K (or V) row
+    switch (d->kv_dtype) {
+        case DA_KV_BF16:
+        case DA_KV_FP8_PER_TENSOR:
+            if (d->D_qk != d->D_v || (d->D_qk % 8) != 0) return DA_ERR_UNSUPPORTED;
+            row_len = (int64_t)d->H_kv * d->D_qk;
+            break;
+        case DA_KV_FP8_MLA656:
+            if (d->H_kv != 1 || d->D_qk != 576 || d->D_v != 512) return DA_ERR_UNSUPPORTED;
+            row_len = 576;
+            break;
+        default:
+            return DA_ERR_UNSUPPORTED;
+    }
+    if (new_row_stride == 0) new_row_stride = row_len;
+    if (new_row_stride < row_len || (new_row_stride % 8) != 0 || new_row_stride > ((int64_t)1 << 40))
+        return DA_ERR_DIMS;
+    if (!k_new || !positions || !block_table || !k_pool) return DA_ERR_NULL;
+    if (mla) {
+        if (v_new) return DA_ERR_UNSUPPORTED;
+        if (v_pool && v_pool != k_pool) return DA_ERR_UNSUPPORTED;
+    } else if (!v_new || !v_pool) {
+        return DA_ERR_NULL;
+    }
+    if (!aligned16(k_new) || (v_new && !aligned16(v_new)) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool)) ||
+        (reinterpret_cast<uintptr_t>(positions) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+        (reinterpret_cast<uintptr_t>(device_error) & 3u))
+        return DA_ERR_ALIGN;
+    if (d->kv_dtype == DA_KV_FP8_PER_TENSOR) {
+        if (!k_scale || !v_scale) return DA_ERR_SCALE;
+        if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+            return DA_ERR_ALIGN;
+    }
+    AppendParams p;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.positions = positions;
+    p.block_table = block_table;
+    p.k_pool = static_cast<uint8_t *>(k_pool);
+    p.v_pool = static_cast<uint8_t *>(mla ? k_pool : v_pool);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.error = device_error;
+    p.row_stride = new_row_stride;
+    p.B = d->B;
+    p.H_kv = d->H_kv;
+    p.D = d->D_qk;
+    p.page_size = d->page_size;
+    p.max_pages = d->max_pages_per_seq;
+    p.num_pages = d->num_pages;
+    if (launch_append(d->kv_dtype, p, stream, true) != cudaSuccess) return DA_ERR_CUDA;
+    return DA_OK;
 }
 
 int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStream_t stream) {

@@ -1,0 +1,200 @@
+// KV append: writes each request's new token into the page slot that its
+// block table gives for its position, quantising on the way.
+//
+// The decode kernels read a pool that already holds the step's new K/V; the
+// write itself happens upstream of attention (XQA page, section
+// "一次 decode step 的完整时序": the KV append is not part of XQA, the new
+// token lands in the pool first and the attention kernel only reads through
+// the page table). The formats are those the decode kernels read:
+//   * bf16 pools: a copy of the token's H_kv * D values;
+//   * e4m3 pools: code = e4m3(x / scale[h]) with one fp32 scale per KV head and
+//     tensor (XQA page, section "Hopper 路径上 V 不做显式反量化", largest finite 448);
+//   * the 656-byte latent token (FlashMLA page, section "数据加载"): per block
+//     of 128 NoPE values, scale = max|x| / 448 (1 for an all-zero block),
+//     512 codes, the four fp32 scales, then the 64 RoPE values as bf16.
+// Rounding is the IEEE one everywhere: the quotient x / scale is an fp32
+// division rounded to nearest (not a multiply by a reciprocal), the e4m3 code
+// the nearest finite value with ties to even, saturating at +-448; NaN maps
+// to 0x7F. The pool layout is [num_pages][page_size][H_kv][D] (bf16 / e4m3)
+// or [num_pages][page_size][1][656].
+//
+// The work is a scatter of a few hundred bytes per request, HBM / latency
+// bound: one 16-byte load and one 16- or 8-byte store per thread, coalesced
+// along the token's contiguous H_kv * D values; the latent format takes one
+// warp per token (lanes 8k..8k+7 own block k and reduce its max with shuffles).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "decode_attn.h"
+#include "layout.h"
+
+namespace da {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLatentRow = 656;
+constexpr int kLatentNope = 512;
+constexpr int kLatentScales = 512;   // byte offset of the 4 fp32 scales
+constexpr int kLatentRope = 528;     // byte offset of the 64 bf16 RoPE values
+constexpr float kE4m3Max = 448.f;
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void *p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> two e4m3 codes (lo in bits 0..7, hi in bits 8..15):
+// round to nearest even, finite results saturate at +-448, NaN -> 0x7F.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    uint32_t c = r;
+    if (lo != lo) c = (c & 0xFF00u) | 0x7Fu;
+    if (hi != hi) c = (c & 0x00FFu) | 0x7F00u;
+    return c;
+}
+
+// Eight bf16 values (one 16-byte vector) / s -> eight e4m3 codes.
+__device__ __forceinline__ uint2 quant8(uint4 x, float s) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// Shared prologue of both kernels: where request b's token goes, or -1 when
+// it is skipped (negative position) or invalid (error bit set by `reporter`).
+__device__ __forceinline__ int64_t slot_of(const AppendParams &p, int b, bool reporter) {
+    const int t = __ldg(p.positions + b);
+    if (t < 0) return -1;
+    if ((int64_t)t >= (int64_t)p.max_pages * p.page_size) {
+        if (reporter && p.error) atomicOr(p.error, DA_DEV_SEQ_TOO_LONG);
+        return -1;
+    }
+    const int page = __ldg(p.block_table + (int64_t)b * p.max_pages + t / p.page_size);
+    if (page < 0 || page >= p.num_pages) {
+        if (reporter && p.error) atomicOr(p.error, DA_DEV_BAD_PAGE);
+        return -1;
+    }
+    return (int64_t)page * p.page_size + t % p.page_size;
+}
+
+// bf16 / e4m3 pools. Work item = one 16-byte vector of 8 values of K or V of
+// one request; items of one request are consecutive (K vectors, then V).
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads) append_gqa_kernel(const AppendParams p) {
+    pdl_wait();               // positions, block table and new rows may come from the previous kernel
+    pdl_launch_dependents();  // the next kernel waits for this grid before it reads the pool
+    const int vpr = p.D >> 3;
+    const int per_tensor = p.H_kv * vpr;
+    const int64_t per_req = 2 * (int64_t)per_tensor;
+    const int64_t total = (int64_t)p.B * per_req;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
+        const int b = (int)(i / per_req);
+        const int r = (int)(i - (int64_t)b * per_req);
+        const int64_t slot = slot_of(p, b, r == 0);
+        if (slot < 0) continue;
+        const bool is_v = r >= per_tensor;
+        const int e = is_v ? r - per_tensor : r;
+        const uint16_t *src = (is_v ? p.v_new : p.k_new) + (int64_t)b * p.row_stride + (int64_t)e * 8;
+        const uint4 x = ld_stream_v4(src);
+        uint8_t *pool = is_v ? p.v_pool : p.k_pool;
+        const int64_t vec = slot * per_tensor + e;
+        if constexpr (!kFp8) {
+            st_v4(pool + vec * 16, x);
+        } else {
+            const float s = __ldg((is_v ? p.v_scale : p.k_scale) + e / vpr);
+            st_v2(pool + vec * 8, quant8(x, s));
+        }
+    }
+}
+
+// 656-byte latent tokens, one warp per request. Lane l holds NoPE values
+// [16l, 16l+16); lanes 8k..8k+7 form block k.
+__global__ void __launch_bounds__(kThreads) append_mla_kernel(const AppendParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    constexpr int kWarps = kThreads / 32;
+    for (int b = blockIdx.x * kWarps + (threadIdx.x >> 5); b < p.B; b += gridDim.x * kWarps) {
+        const int64_t slot = slot_of(p, b, lane == 0);   // uniform over the warp
+        if (slot < 0) continue;
+        const uint16_t *src = p.k_new + (int64_t)b * p.row_stride;
+        const uint4 a0 = ld_stream_v4(src + lane * 16);
+        const uint4 a1 = ld_stream_v4(src + lane * 16 + 8);
+        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        // max |x| by the magnitude bits: exact, and a NaN wins (scale 1 then)
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            m = max(m, (w[i] << 16) & 0x7FFFFFFFu);
+            m = max(m, w[i] & 0x7FFF0000u);
+        }
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        const float amax = __uint_as_float(m);
+        const float scale = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
+            const uint32_t hi =
+                e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
+            c[i] = lo | (hi << 16);
+        }
+        uint8_t *row = p.k_pool + slot * kLatentRow;
+        st_v4(row + lane * 16, make_uint4(c[0], c[1], c[2], c[3]));
+        const float s1 = __shfl_sync(0xFFFFFFFFu, scale, 8);
+        const float s2 = __shfl_sync(0xFFFFFFFFu, scale, 16);
+        const float s3 = __shfl_sync(0xFFFFFFFFu, scale, 24);
+        if (lane == 0)
+            st_v4(row + kLatentScales,
+                  make_uint4(__float_as_uint(scale), __float_as_uint(s1), __float_as_uint(s2), __float_as_uint(s3)));
+        if (lane < 8) st_v4(row + kLatentRope + lane * 16, ld_stream_v4(src + kLatentNope + lane * 8));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stream, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    constexpr int64_t kMaxBlocks = 152 * 16;   // grid-stride beyond 16 CTAs per SM
+    if (kv_dtype == DA_KV_FP8_MLA656) {
+        const int64_t blocks = (p.B + kThreads / 32 - 1) / (kThreads / 32);
+        cfg.gridDim = dim3((unsigned)(blocks < kMaxBlocks ? blocks : kMaxBlocks));
+        return cudaLaunchKernelEx(&cfg, append_mla_kernel, p);
+    }
+    const int64_t items = (int64_t)p.B * 2 * p.H_kv * (p.D / 8);
+    const int64_t blocks = (items + kThreads - 1) / kThreads;
+    cfg.gridDim = dim3((unsigned)(blocks < kMaxBlocks ? blocks : kMaxBlocks));
+    if (kv_dtype == DA_KV_FP8_PER_TENSOR) return cudaLaunchKernelEx(&cfg, append_gqa_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, append_gqa_kernel<false>, p);
+}
+
+}  // namespace da

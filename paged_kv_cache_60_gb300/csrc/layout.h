@@ -112,4 +112,16 @@ struct CombineParams {
     int32_t B, H_q, D_v, H_kv, G, splits, num_parts;
 };
 
+struct AppendParams {
+    const uint16_t *k_new;         // bf16 rows, request b at k_new + b * row_stride
+    const uint16_t *v_new;         // same layout (unused for the 656-byte token)
+    const int32_t *positions;      // [B]; < 0: request skipped
+    const int32_t *block_table;    // [B][max_pages]
+    uint8_t *k_pool, *v_pool;
+    const float *k_scale, *v_scale;  // [H_kv], e4m3 pools only
+    int32_t *error;                // device word, error bits OR-ed in; may be null
+    int64_t row_stride;            // bf16 elements between consecutive requests of k_new / v_new
+    int32_t B, H_kv, D, page_size, max_pages, num_pages;
+};
+
 }  // namespace da

@@ -100,3 +100,29 @@ def test_fwd_rejects_null_and_misaligned_before_launch(lib):
 def test_strerror_is_total(lib):
     for c in range(-10, 2):
         assert isinstance(da.strerror(c), str) and da.strerror(c)
+
+
+def test_append_rejects_bad_arguments_before_launch(lib):
+    P = ctypes.c_void_p
+    g = P(0x10000)
+    f = lib.decode_attn_append_kv
+
+    def call(d, k_new=g, v_new=g, stride=0, pos=g, bt=g, kp=g, vp=g, ks=None, vs=None, err=None):
+        return f(ctypes.byref(d), k_new, v_new, stride, pos, bt, kp, vp, ks, vs, err, None)
+
+    d = _desc()
+    assert call(d, k_new=None) == -1
+    assert call(d, v_new=None) == -1
+    assert call(d, vp=None) == -1
+    assert call(d, k_new=P(0x10008)) == -4
+    assert call(d, err=P(0x10002)) == -4
+    assert call(d, stride=100) == -2            # below the row of H_kv * D values
+    assert call(d, stride=2 * 128 + 4) == -2    # not a multiple of 8 elements
+    assert call(_desc(D_qk=100, D_v=100)) == -3
+    assert call(_desc(D_qk=128, D_v=64)) == -3
+    assert call(_desc(B=0)) == -2
+    assert call(_desc(kv_dtype=da.KV_FP8)) == -8
+    dm = _desc(kv_dtype=da.KV_MLA656, H_kv=1, G=128, D_qk=576, D_v=512)
+    assert call(dm) == -3                        # the latent token takes no v_new
+    assert call(dm, v_new=None, vp=P(0x20000)) == -3
+    assert call(_desc(kv_dtype=da.KV_MLA656, H_kv=2, G=128, D_qk=576, D_v=512), v_new=None, vp=None) == -3

@@ -250,3 +250,18 @@ def repermute_pages(w: Workload, seed: int) -> Workload:
                     k_pool=move(w.k_pool), v_pool=move(w.v_pool),
                     k_scale=w.k_scale, v_scale=w.v_scale,
                     block_table=bt.to(torch.int32), cache_seqlens=w.cache_seqlens.clone())
+
+
+def make_append_batch(w: Workload, seed: int):
+    """Inputs of a KV append on workload ``w``: one new token per request,
+    written at the slot of its last token (positions[b] = lengths[b] - 1, -1
+    for an empty request, which the append skips). Returns (k_new, v_new,
+    positions): bf16 N(0,1) rows [B, H_kv, D_qk] and [B, H_kv, D_v] like the
+    pools' values, or for the 656-byte format the 576-value latent vector in
+    k_new and v_new None; positions int32 [B]."""
+    s = w.spec
+    gen = torch.Generator().manual_seed(seed)
+    k_new = _randn(gen, (s.B, s.H_kv, s.D_qk)).to(torch.bfloat16)
+    v_new = None if s.kv_dtype == KV_MLA656 else _randn(gen, (s.B, s.H_kv, s.D_v)).to(torch.bfloat16)
+    positions = torch.tensor([L - 1 for L in w.lengths], dtype=torch.int32)
+    return k_new, v_new, positions
