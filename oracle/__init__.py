@@ -6,6 +6,8 @@ benchmark's CPU-baseline leg may import this package; the library under
 
 * ``decode_ref.c``  -- attention by its definition, per (request, KV head,
   head range, token range), plus the split merge; built with gcc + OpenMP.
+  ``attend_multi`` applies it per draft token for several query tokens per
+  request (each draft sees the history and the drafts before it).
 * ``sched_ref.py``  -- the integer split-KV scheduling metadata.
 * ``append_ref.py`` -- appending one new token per request into its page slot,
   with the e4m3 encoder (per-head scales, or the 656-byte latent token).
@@ -136,6 +138,30 @@ def attend(w, heads=None):
     for i, (b, h) in enumerate(heads):
         out[b, h * s.G:(h + 1) * s.G] = o[i]
         lse[b, h * s.G:(h + 1) * s.G] = l[i]
+    return out, lse
+
+
+def attend_multi(w, heads=None):
+    """Several query tokens per request (linear speculative-decoding
+    verification, XQA page, section "投机解码:XQA 的第二个工作负载": the drafts
+    form a chain, so each sees the history and the drafts before it). The
+    request's last s_q tokens are the drafts, already in the cache (L_b counts
+    them); draft j attends over tokens [0, L_b - s_q + 1 + j). w.q is
+    [B, s_q, H_q, D_qk]. Returns out [B, s_q, H_q, D_v] and lse [B, s_q, H_q]
+    (float64; NaN where not computed; lse -inf for a draft that sees nothing)."""
+    s = w.spec
+    sq = s.s_q
+    if heads is None:
+        heads = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
+    out = torch.full((s.B, sq, s.H_q, s.D_v), float("nan"), dtype=torch.float64)
+    lse = torch.full((s.B, sq, s.H_q), float("nan"), dtype=torch.float64)
+    q = w.q.view(s.B, sq, s.H_q, s.D_qk)
+    for j in range(sq):
+        units = [(b, h, 0, s.G, 0, max(0, w.lengths[b] - sq + 1 + j)) for (b, h) in heads]
+        o, l = attend_units(w, units, q64=q[:, j].to(torch.float64).contiguous())
+        for i, (b, h) in enumerate(heads):
+            out[b, j, h * s.G:(h + 1) * s.G] = o[i]
+            lse[b, j, h * s.G:(h + 1) * s.G] = l[i]
     return out, lse
 
 

@@ -35,6 +35,7 @@ class WorkloadSpec:
     extra_pages: int = 0                # unused pages in the pool (poisoned)
     softmax_scale: float = 0.0          # 0 = 1/sqrt(D_qk)
     seed: int = 0
+    s_q: int = 1                        # query tokens per request (draft tokens of a linear chain)
     description: str = field(default="", compare=False)
 
     @property

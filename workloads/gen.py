@@ -149,7 +149,9 @@ def make_workload(spec: WorkloadSpec, lengths: Optional[List[int]] = None,
     bt, num_pages, maxp = build_block_table(spec, lengths)
     gen = torch.Generator().manual_seed(spec.seed)
 
-    q = _randn(gen, (B, H_q, Dq)).to(torch.bfloat16)
+    # one query token per request: q [B, H_q, D_qk]; s_q > 1: q [B, s_q, H_q, D_qk]
+    q_shape = (B, H_q, Dq) if spec.s_q == 1 else (B, spec.s_q, H_q, Dq)
+    q = _randn(gen, q_shape).to(torch.bfloat16)
     valid = valid_slot_mask(spec, lengths, bt, num_pages) if poison else None
     k_scale = v_scale = None
     v_pool = None
