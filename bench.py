@@ -169,7 +169,7 @@ def make_desc(da, w):
     s = w.spec
     return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,
                         max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=s.kv_dtype,
-                        splits=s.splits, softmax_scale=s.softmax_scale)
+                        splits=s.splits, softmax_scale=s.softmax_scale, s_q=s.s_q)
 
 
 class DevCopy:
@@ -184,8 +184,8 @@ class DevCopy:
         self.cache_seqlens = w.cache_seqlens.to(dev)
         s = w.spec
         self.meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device=dev)
-        self.out = torch.empty(s.B, s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty(s.B, s.H_q, dtype=torch.float32, device=dev)
+        self.out = torch.empty(s.B, s.s_q * s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(s.B, s.s_q * s.H_q, dtype=torch.float32, device=dev)
         # one new token per request, written at its last position (decode_attn_append_kv)
         from workloads import make_append_batch
         k_new, v_new, pos = make_append_batch(w, seed=s.seed + 1)
@@ -214,13 +214,14 @@ def oracle_time_per_call(w, budget_s):
     units, scaled to one whole call. Returns (us_per_call, cores, sample text)."""
     import oracle
     s = w.spec
+    attend = oracle.attend_multi if s.s_q > 1 else oracle.attend
     units_all = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
     cost = {u: w.lengths[u[0]] for u in units_all}
     total_cost = sum(cost.values())
     # cheap probe on the shortest unit to size the sample
     probe = min(units_all, key=lambda u: cost[u])
     t0 = time.perf_counter()
-    oracle.attend(w, heads=[probe])
+    attend(w, heads=[probe])
     t_probe = max(time.perf_counter() - t0, 1e-6)
     per_token = t_probe / max(1, cost[probe])
     cores = oracle.num_threads()
@@ -234,10 +235,10 @@ def oracle_time_per_call(w, budget_s):
             break
     reps = 1
     t0 = time.perf_counter()
-    oracle.attend(w, heads=sample)
+    attend(w, heads=sample)
     el = time.perf_counter() - t0
     while el * (reps + 1) / reps < budget_s and reps < 1000:
-        oracle.attend(w, heads=sample)
+        attend(w, heads=sample)
         reps += 1
         el = time.perf_counter() - t0
     sample_cost = sum(cost[u] for u in sample)
@@ -470,7 +471,8 @@ def run_ours(args, rank, world, local):
             "dtype": {da.KV_BF16: "bf16", da.KV_FP8: "fp8-e4m3 kv / bf16 q,out"}.get(
                 spec.kv_dtype, "fp8-e4m3 656-byte kv dequantised to bf16 / bf16 q,out"),
             "data": "synthetic",
-            "config": {"workload": args.workload, "desc": spec.description, "B": spec.B, "H_q": spec.H_q,
+            "config": {"workload": args.workload, "desc": spec.description, "B": spec.B, "s_q": spec.s_q,
+                       "H_q": spec.H_q,
                        "H_kv": spec.H_kv, "D_qk": spec.D_qk, "D_v": spec.D_v, "page_size": spec.page_size,
                        "splits": spec.splits, "kv_bytes_per_call": kv_bytes,
                        "l2": ("inputs rotate over %d copies (%.0f MB > 2x L2)" % (copies, copies * kv_bytes / 1e6))

@@ -76,13 +76,14 @@ typedef struct {
     int32_t splits;            /* 0: balanced over the SMs; S > 0: S splits per request */
     int32_t num_sms;           /* 0: query the current device */
     float softmax_scale;       /* sigma; 0: 1/sqrt(D_qk) */
+    int32_t s_q;               /* query tokens per request (0 means 1); see decode_attn_fwd */
 } da_desc;
 
 /* Return codes. */
 #define DA_OK                  0
 #define DA_ERR_NULL           -1   /* a required pointer is NULL */
 #define DA_ERR_DIMS           -2   /* a size is out of range */
-#define DA_ERR_UNSUPPORTED    -3   /* no kernel for this (dtype, D_qk, D_v, G, page_size) */
+#define DA_ERR_UNSUPPORTED    -3   /* no kernel for this (dtype, D_qk, D_v, G, page_size, s_q) */
 #define DA_ERR_ALIGN          -4   /* a pointer is not 16-byte aligned */
 #define DA_ERR_SPLITS         -5   /* splits < 0 or too large */
 #define DA_ERR_META_SIZE      -6   /* sched_meta buffer smaller than decode_attn_sched_meta_bytes */
@@ -100,7 +101,7 @@ typedef struct {
  * Size in bytes of the sched_meta buffer for this desc (host only, no CUDA
  * call except an SM-count query when desc->num_sms is 0). The buffer holds the
  * scheduling metadata, the split-KV partials (fp32 o and lse per split and
- * query head), the device error word and, for DA_KV_FP8_MLA656, the slots in
+ * output row: query token x query head), the device error word and, for DA_KV_FP8_MLA656, the slots in
  * which the two CTAs of a part swap their partial scores (32 KB per CTA;
  * rewritten by every decode_attn_fwd, never read across calls).
  */
@@ -111,7 +112,7 @@ int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
  * header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part,
  * total size. Header (16 int32): magic, B, H_kv, G, splits, num_parts, cpc,
  * chunk (64), total_chunks, total_splits, per, error word, error detail,
- * kv_dtype, num_sms, reserved. parts: num_parts records of 8 int32
+ * kv_dtype, num_sms, s_q. parts: num_parts records of 8 int32
  * {b0, s0, c0, c1, co0, L0, so0, ns0}: first request, its split index there,
  * global chunk interval [c0, c1), then chunk_offset[b0], min(L_b0,
  * max_pages_per_seq*page_size), split_offset[b0], num_splits[b0] (all 0 when
@@ -142,6 +143,17 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
 /*
  * Decode attention forward. Launches the split-KV kernel and the LSE combine
  * kernel (chained with programmatic dependent launch) on `stream`.
+ *
+ * Several query tokens per request (desc->s_q > 1) verify a chain of draft
+ * tokens (XQA page, section "投机解码:XQA 的第二个工作负载", the linear case;
+ * FlashMLA's call passes s_q * h_q / h_kv rows per KV head): the request's
+ * last s_q tokens are already in the pool (L_b counts them) and draft token
+ * j < s_q sees the first L_b - s_q + 1 + j tokens -- the history and the
+ * drafts up to itself. A row that sees no token gets out = 0, lse = -inf.
+ * Supported: s_q <= 4 for bf16 D = 64, s_q <= 2 for D = 128 (bf16, e4m3);
+ * the 656-byte format takes s_q = 1. The rows of q, out and lse below are
+ * then [B][s_q][H_kv*G]; the scheduling metadata must be built with the same s_q.
+ *
  *   q:            bf16 [B][H_kv*G][D_qk], query head h*G+g belongs to KV head h
  *   k_pool/v_pool: see da_kv_dtype
  *   k_scale/v_scale: fp32 [H_kv] for DA_KV_FP8_PER_TENSOR, else ignored

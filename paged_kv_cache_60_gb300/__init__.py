@@ -37,13 +37,13 @@ class Desc(ctypes.Structure):
                 ("D_qk", ctypes.c_int32), ("D_v", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("s_q", ctypes.c_int32)]
 
     @classmethod
     def make(cls, B, H_kv, G, D_qk, D_v, page_size, max_pages_per_seq, num_pages, kv_dtype=KV_BF16,
-             splits=0, num_sms=0, softmax_scale=0.0):
+             splits=0, num_sms=0, softmax_scale=0.0, s_q=1):
         return cls(B, H_kv, G, D_qk, D_v, page_size, max_pages_per_seq, num_pages, kv_dtype, splits,
-                   num_sms, softmax_scale)
+                   num_sms, softmax_scale, s_q)
 
 
 class LaunchOpts(ctypes.Structure):

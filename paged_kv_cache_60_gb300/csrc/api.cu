@@ -33,6 +33,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool is_mla(const da_desc *d) { return d->kv_dtype == DA_KV_FP8_MLA656; }
 
+// query tokens per request (0 in the desc means 1)
+int sq_of(const da_desc *d) { return d->s_q <= 0 ? 1 : d->s_q; }
+
 // Which kernel serves this desc; returns DA_OK or an error code.
 int check_desc(const da_desc *d) {
     if (!d) return DA_ERR_NULL;
@@ -44,18 +47,23 @@ int check_desc(const da_desc *d) {
     if (d->splits < 0 || d->splits > 4096) return DA_ERR_SPLITS;
     if (d->num_sms < 0) return DA_ERR_DIMS;
     if (!(d->softmax_scale >= 0.f) || std::isinf(d->softmax_scale)) return DA_ERR_DIMS;
+    if (d->s_q < 0 || d->s_q > 64) return DA_ERR_DIMS;
+    const int sq = sq_of(d);
     const int P = d->page_size;
     const bool page_ok = (P == 8 || P == 16 || P == 32 || (P % 64) == 0);
     if (!page_ok) return DA_ERR_UNSUPPORTED;
     switch (d->kv_dtype) {
         case DA_KV_BF16:
             if (d->G != 8 || d->D_qk != d->D_v || (d->D_qk != 64 && d->D_qk != 128)) return DA_ERR_UNSUPPORTED;
+            if (sq > (d->D_qk == 64 ? kMaxSqD64 : kMaxSqD128)) return DA_ERR_UNSUPPORTED;
             break;
         case DA_KV_FP8_PER_TENSOR:
             if (d->G != 8 || d->D_qk != 128 || d->D_v != 128) return DA_ERR_UNSUPPORTED;
+            if (sq > kMaxSqD128) return DA_ERR_UNSUPPORTED;
             break;
         case DA_KV_FP8_MLA656:
             if (d->H_kv != 1 || d->D_qk != 576 || d->D_v != 512 || d->G != 128) return DA_ERR_UNSUPPORTED;
+            if (sq != 1) return DA_ERR_UNSUPPORTED;
             if (!mla_kernel_available()) return DA_ERR_UNSUPPORTED;
             break;
         default:
@@ -109,6 +117,7 @@ int make_layout(const da_desc *d, MetaLayout *L) {
     }
     if (num_parts > (1 << 24)) return DA_ERR_SPLITS;
     const int64_t H_q = (int64_t)d->H_kv * d->G;
+    const int64_t rows = H_q * sq_of(d);  // output rows per request
     size_t off = 0;
     L->header = off;
     off += kHeaderWords * 4;
@@ -122,9 +131,9 @@ int make_layout(const da_desc *d, MetaLayout *L) {
     off += round_up((size_t)d->B * 4, 16);
     off = round_up(off, 256);
     L->lse_part = off;
-    off += round_up((size_t)max_splits * H_q * 4, 256);
+    off += round_up((size_t)max_splits * rows * 4, 256);
     L->o_part = off;
-    off += round_up((size_t)max_splits * H_q * d->D_v * 4, 256);
+    off += round_up((size_t)max_splits * rows * d->D_v * 4, 256);
     L->xchg = off;  // per part, per CTA of the pair: 128 heads x 64 tokens fp32
     if (is_mla(d)) off += round_up((size_t)num_parts * 2 * H_q * kChunk * 4, 256);
     L->total = off;
@@ -259,6 +268,7 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens, vo
     p.max_len = desc->max_pages_per_seq * desc->page_size;
     p.kv_dtype = desc->kv_dtype;
     p.num_sms = nsm;
+    p.s_q = sq_of(desc);
     if (launch_sched_meta(p, stream, true) != cudaSuccess) return DA_ERR_CUDA;
     return DA_OK;
 }
@@ -322,6 +332,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.H_kv = desc->H_kv;
         p.G = desc->G;
         p.H_q = H_q;
+        p.s_q = sq_of(desc);
         p.max_pages = desc->max_pages_per_seq;
         p.num_pages = desc->num_pages;
         p.page_size = P;
@@ -368,7 +379,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
     c.out = out;
     c.lse = lse;
     c.B = desc->B;
-    c.H_q = H_q;
+    c.rows = H_q * sq_of(desc);
+    c.s_q = sq_of(desc);
     c.D_v = desc->D_v;
     c.H_kv = desc->H_kv;
     c.G = desc->G;

@@ -8,7 +8,8 @@
 // result is bitwise reproducible. The kernel is chained to the split-KV kernel
 // with programmatic dependent launch (FlashMLA page, section "合并与性能账本").
 //
-// One warp per query head; each lane owns DV/32 consecutive outputs.
+// One warp per output row (query token, query head); each lane owns DV/32
+// consecutive outputs.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -29,36 +30,36 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     const int ns = p.meta.num_splits[b];
     const int so = p.meta.split_offset[b];
     if (!(hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv && hd[kHG] == p.G &&
-          hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts))
+          hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts && hd[kHSq] == p.s_q))
         return;  // the split-KV kernel has flagged the mismatch
-    if (hq >= p.H_q) return;
+    if (hq >= p.rows) return;
     if (ns == 1) return;  // written directly by the split-KV kernel
     if (ns < 0 || so < 0 || so + ns > p.meta.max_splits) return;
     constexpr int PER_LANE = DV / 32;
     static_assert(DV % 64 == 0, "DV must be a multiple of 64");
-    const float *lp = p.meta.lse_part + (size_t)so * p.H_q + hq;
+    const float *lp = p.meta.lse_part + (size_t)so * p.rows + hq;
     // lane s holds split s's lse (splits beyond 32 are folded in a loop)
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, lp[(size_t)s * p.H_q]);
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, lp[(size_t)s * p.rows]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)b * p.H_q + hq) * DV;
+    __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)b * p.rows + hq) * DV;
     float acc[PER_LANE];
 #pragma unroll
     for (int k = 0; k < PER_LANE; ++k) acc[k] = 0.f;
     float lse_v = -INFINITY;
     if (M != -INFINITY) {
         float Z = 0.f;
-        for (int s = lane; s < ns; s += 32) Z += ex2((lp[(size_t)s * p.H_q] - M) * kLog2e);
+        for (int s = lane; s < ns; s += 32) Z += ex2((lp[(size_t)s * p.rows] - M) * kLog2e);
         // fixed-order tree sum over lanes
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
         lse_v = M + logf(Z);
         for (int s0 = 0; s0 < ns; s0 += 32) {
             const int cnt = min(32, ns - s0);
-            const float w_l = (lane < cnt) ? ex2((lp[(size_t)(s0 + lane) * p.H_q] - lse_v) * kLog2e) : 0.f;
-            const float *src0 = p.meta.o_part + (((size_t)(so + s0)) * p.H_q + hq) * DV;
-            const size_t sstride = (size_t)p.H_q * DV;
+            const float w_l = (lane < cnt) ? ex2((lp[(size_t)(s0 + lane) * p.rows] - lse_v) * kLog2e) : 0.f;
+            const float *src0 = p.meta.o_part + (((size_t)(so + s0)) * p.rows + hq) * DV;
+            const size_t sstride = (size_t)p.rows * DV;
 #pragma unroll 4
             for (int s = 0; s < cnt; ++s) {
                 const float w = __shfl_sync(0xffffffffu, w_l, s);
@@ -91,12 +92,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
             reinterpret_cast<uint2 *>(op)[k4 * 32 + lane] = w;
         }
     }
-    if (lane == 0) p.lse[(size_t)b * p.H_q + hq] = lse_v;
+    if (lane == 0) p.lse[(size_t)b * p.rows + hq] = lse_v;
 }
 
 cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.B, (p.H_q + 3) / 4);
+    cfg.gridDim = dim3(p.B, (p.rows + 3) / 4);
     cfg.blockDim = dim3(128);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

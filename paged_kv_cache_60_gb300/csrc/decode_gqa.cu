@@ -29,6 +29,11 @@
 //    two values per cvt; the per-tensor scales are folded into the score scale
 //    (k_scale) and into the output (v_scale) (same page, section
 //    "Hopper 路径上 V 不做显式反量化").
+//  * several query tokens per request (linear speculative-decoding
+//    verification, XQA page, section "投机解码:XQA 的第二个工作负载"): the
+//    s_q draft tokens' G heads become NQ n8 tiles on the N side, so every K/V
+//    fragment loaded from shared memory feeds NQ MMAs; draft token j sees the
+//    tokens [0, L - s_q + j] (a chain: each draft token sees the ones before it).
 //  * every consumer warp takes whole chunks (round robin) as four independent
 //    16-token tiles, so its MMA chains and shuffle reductions interleave, and
 //    keeps its own (m, l, O) state; at the end of a segment the warps' states are merged
@@ -79,8 +84,10 @@ struct GqaCfg {
     static_assert(!FP8 || NX == 1, "fp8 path expects one 128-byte box per row");
 };
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_BLOCKS)
+// NQ: query tokens per request the kernel is compiled for (s_q <= NQ; tokens
+// j >= s_q are zero rows that are never written).
+template <int D, bool FP8, int NQ>
+__global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, (NQ == 1) ? GqaCfg<D, FP8>::MIN_BLOCKS : 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ GqaParams p) {
     using C = GqaCfg<D, FP8>;
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         const int32_t *hd = p.meta.header;
         const bool ok = hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv &&
                         hd[kHG] == p.G && hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts &&
-                        (int)gridDim.x == p.num_parts;
+                        hd[kHSq] == p.s_q && (int)gridDim.x == p.num_parts;
         if (!ok) {
             if (threadIdx.x == 0) atomicOr(&p.meta.header[kHError], DA_DEV_META_MISMATCH);
             return;
@@ -248,17 +255,24 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
     Seg sg;
     while (wk.next(sg)) {
         const int sb = sg.b, ss = sg.s, lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
-        // query fragments (B operand, n = query head r8 of this group)
-        uint32_t qf[C::KS][2];
-        {
-            const size_t qrow = ((size_t)sb * p.H_q + (size_t)h * C::G + r8) * D;
+        // query fragments (B operand, n = query head r8 of this group), one
+        // n8 tile per query token of the request; q is [B][s_q][H_q][D]
+        uint32_t qf[C::KS][NQ][2];
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+            if (j >= p.s_q) {
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) qf[ks][j][0] = qf[ks][j][1] = 0u;
+                continue;
+            }
+            const size_t qrow = (((size_t)sb * p.s_q + j) * p.H_q + (size_t)h * C::G + r8) * D;
             if constexpr (!FP8) {
                 const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
                     reinterpret_cast<const __nv_bfloat16 *>(p.q) + qrow);
 #pragma unroll
                 for (int ks = 0; ks < C::KS; ++ks) {
-                    qf[ks][0] = q32[ks * 8 + c4];
-                    qf[ks][1] = q32[ks * 8 + 4 + c4];
+                    qf[ks][j][0] = q32[ks * 8 + c4];
+                    qf[ks][j][1] = q32[ks * 8 + 4 + c4];
                 }
             } else {
                 const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(p.q) + qrow;
@@ -267,15 +281,22 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                     const uint2 v = *reinterpret_cast<const uint2 *>(qb + ks * 16 + c4 * 4);
                     const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
                     const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
-                    qf[ks][0] = pack_f16(__low2float(lo), __high2float(lo));
-                    qf[ks][1] = pack_f16(__low2float(hi), __high2float(hi));
+                    qf[ks][j][0] = pack_f16(__low2float(lo), __high2float(lo));
+                    qf[ks][j][1] = pack_f16(__low2float(hi), __high2float(hi));
                 }
             }
         }
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float acc[C::MT][4];
+        // draft token j sees the first L - s_q + 1 + j tokens
+        const int L_first = L - p.s_q + 1;
+        float m0[NQ], m1[NQ], l0[NQ], l1[NQ];
+        float acc[C::MT][NQ][4];
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        for (int j = 0; j < NQ; ++j) {
+            m0[j] = m1[j] = -INFINITY;
+            l0[j] = l1[j] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) acc[mt][j][0] = acc[mt][j][1] = acc[mt][j][2] = acc[mt][j][3] = 0.f;
+        }
 
         for (int lc = lc0; lc < lc1; ++lc, ++i) {
             if ((i % C::NCW) != warp) continue;  // one warp per chunk, round robin
@@ -298,7 +319,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 }
                 break;
             }
-            const int nvalid = L - lc * kChunk;  // >= 1: valid tokens of this chunk
+            const int nvalid = L - lc * kChunk;  // >= 1: tokens of this chunk the last draft token sees
             uint8_t *stage_ptr = smem + (size_t)stage * C::STAGE;
             const uint32_t s_base = smem_u32(stage_ptr);
             const bool tail = nvalid < kChunk;
@@ -314,9 +335,11 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                 __syncwarp();
             }
             // ---- S^T = K Q^T for four independent 16-token tiles
-            float sacc[4][4];
+            float sacc[4][NQ][4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int j = 0; j < NQ; ++j) sacc[t][j][0] = sacc[t][j][1] = sacc[t][j][2] = sacc[t][j][3] = 0.f;
             if constexpr (!FP8) {
 #pragma unroll
                 for (int ks = 0; ks < C::KS; ++ks) {
@@ -327,7 +350,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                         const uint32_t addr = s_base + rk[t] + x * 128 + ((((d & 63) >> 3) ^ (keyk[t] + x)) << 4);
                         uint32_t a[4];
                         ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-                        mma_bf16(sacc[t], a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+                        for (int j = 0; j < NQ; ++j) mma_bf16(sacc[t][j], a, qf[ks][j][0], qf[ks][j][1]);
                     }
                 }
             } else {
@@ -347,53 +371,63 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                             a[1] = e4m3x2_to_f16x2((uint16_t)(rb & 0xffff));
                             a[2] = e4m3x2_to_f16x2((uint16_t)(ra >> 16));
                             a[3] = e4m3x2_to_f16x2((uint16_t)(rb >> 16));
-                            mma_f16(sacc[t], a, qf[kk * 2 + hf][0], qf[kk * 2 + hf][1]);
+#pragma unroll
+                            for (int j = 0; j < NQ; ++j)
+                                mma_f16(sacc[t][j], a, qf[kk * 2 + hf][j][0], qf[kk * 2 + hf][j][1]);
                         }
                     }
                 }
             }
             // ---- online softmax over the chunk's 64 tokens (rows 16t + r8, 16t + r8 + 8)
-            float sv[4][4];
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            uint32_t pb[4][NQ][2];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const bool va = 16 * t + r8 < nvalid, vb = 16 * t + r8 + 8 < nvalid;
-                sv[t][0] = va ? sacc[t][0] * sl2 : -INFINITY;
-                sv[t][1] = va ? sacc[t][1] * sl2 : -INFINITY;
-                sv[t][2] = vb ? sacc[t][2] * sl2 : -INFINITY;
-                sv[t][3] = vb ? sacc[t][3] * sl2 : -INFINITY;
-                mx0 = fmaxf(mx0, fmaxf(sv[t][0], sv[t][2]));
-                mx1 = fmaxf(mx1, fmaxf(sv[t][1], sv[t][3]));
-            }
-            const float mn0 = fmaxf(m0, warp_max_xor_4_8_16(mx0));
-            const float mn1 = fmaxf(m1, warp_max_xor_4_8_16(mx1));
-            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-            float ps0 = 0.f, ps1 = 0.f;
-            uint32_t pb[4][2];
+            for (int j = 0; j < NQ; ++j) {
+                const int nv = (NQ == 1) ? nvalid : L_first + j - lc * kChunk;
+                float sv[4][4];
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float p0 = ex2(sv[t][0] - mn0), p1 = ex2(sv[t][1] - mn1);
-                const float p2 = ex2(sv[t][2] - mn0), p3 = ex2(sv[t][3] - mn1);
-                ps0 += p0 + p2;
-                ps1 += p1 + p3;
-                if constexpr (!FP8) {
-                    pb[t][0] = movmatrix_t(pack_bf16(p0, p1));
-                    pb[t][1] = movmatrix_t(pack_bf16(p2, p3));
-                } else {
-                    pb[t][0] = movmatrix_t(pack_f16(p0, p1));
-                    pb[t][1] = movmatrix_t(pack_f16(p2, p3));
+                for (int t = 0; t < 4; ++t) {
+                    const bool va = 16 * t + r8 < nv, vb = 16 * t + r8 + 8 < nv;
+                    sv[t][0] = va ? sacc[t][j][0] * sl2 : -INFINITY;
+                    sv[t][1] = va ? sacc[t][j][1] * sl2 : -INFINITY;
+                    sv[t][2] = vb ? sacc[t][j][2] * sl2 : -INFINITY;
+                    sv[t][3] = vb ? sacc[t][j][3] * sl2 : -INFINITY;
+                    mx0 = fmaxf(mx0, fmaxf(sv[t][0], sv[t][2]));
+                    mx1 = fmaxf(mx1, fmaxf(sv[t][1], sv[t][3]));
                 }
-            }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
-            m0 = mn0;
-            m1 = mn1;
+                const float mn0 = fmaxf(m0[j], warp_max_xor_4_8_16(mx0));
+                const float mn1 = fmaxf(m1[j], warp_max_xor_4_8_16(mx1));
+                // an earlier draft token may have seen no token yet: keep the
+                // exponent base finite so that 2^(-inf - base) = 0, not NaN
+                const float bs0 = (NQ > 1 && mn0 == -INFINITY) ? 0.f : mn0;
+                const float bs1 = (NQ > 1 && mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = ex2(m0[j] - bs0), al1 = ex2(m1[j] - bs1);
+                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                acc[mt][0] *= al0;
-                acc[mt][1] *= al1;
-                acc[mt][2] *= al0;
-                acc[mt][3] *= al1;
+                for (int t = 0; t < 4; ++t) {
+                    const float p0 = ex2(sv[t][0] - bs0), p1 = ex2(sv[t][1] - bs1);
+                    const float p2 = ex2(sv[t][2] - bs0), p3 = ex2(sv[t][3] - bs1);
+                    ps0 += p0 + p2;
+                    ps1 += p1 + p3;
+                    if constexpr (!FP8) {
+                        pb[t][j][0] = movmatrix_t(pack_bf16(p0, p1));
+                        pb[t][j][1] = movmatrix_t(pack_bf16(p2, p3));
+                    } else {
+                        pb[t][j][0] = movmatrix_t(pack_f16(p0, p1));
+                        pb[t][j][1] = movmatrix_t(pack_f16(p2, p3));
+                    }
+                }
+                l0[j] = l0[j] * al0 + ps0;
+                l1[j] = l1[j] * al1 + ps1;
+                m0[j] = mn0;
+                m1[j] = mn1;
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    acc[mt][j][0] *= al0;
+                    acc[mt][j][1] *= al1;
+                    acc[mt][j][2] *= al0;
+                    acc[mt][j][3] *= al1;
+                }
             }
             // ---- O^T += V^T P^T
             if constexpr (!FP8) {
@@ -406,7 +440,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                         const uint32_t addr = s_base + rv[t] + x * 128 + ((((d & 63) >> 3) ^ (keyv[t] + x)) << 4);
                         uint32_t a[4];
                         ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
-                        mma_bf16(acc[mt], a, pb[t][0], pb[t][1]);
+#pragma unroll
+                        for (int j = 0; j < NQ; ++j) mma_bf16(acc[mt][j], a, pb[t][j][0], pb[t][j][1]);
                     }
                 }
             } else {
@@ -428,7 +463,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
                             a[1] = e4m3x2_to_f16x2((uint16_t)(u >> 16));
                             a[2] = e4m3x2_to_f16x2((uint16_t)(w & 0xffff));
                             a[3] = e4m3x2_to_f16x2((uint16_t)(w >> 16));
-                            mma_f16(acc[kk * 2 + hf], a, pb[t][0], pb[t][1]);
+#pragma unroll
+                            for (int j = 0; j < NQ; ++j) mma_f16(acc[kk * 2 + hf][j], a, pb[t][j][0], pb[t][j][1]);
                         }
                     }
                 }
@@ -439,76 +475,83 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, GqaCfg<D, FP8>::MIN_B
         }
 
         // ---------------------------------------------------------- merge warps
-        l0 = warp_sum_xor_4_8_16(l0);
-        l1 = warp_sum_xor_4_8_16(l1);
-        if (lane < 4) {
-            sm_m[warp * C::G + 2 * c4] = m0;
-            sm_m[warp * C::G + 2 * c4 + 1] = m1;
-            sm_l[warp * C::G + 2 * c4] = l0;
-            sm_l[warp * C::G + 2 * c4 + 1] = l1;
-        }
-        float *uw = sm_u + (size_t)warp * C::G * C::UPAD;
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-            // accumulator rows -> head-dim index
-            const int dA = FP8 ? mt * 16 + 2 * r8 : mt * 16 + r8;
-            const int dB = FP8 ? dA + 1 : dA + 8;
-            uw[(2 * c4) * C::UPAD + dA] = acc[mt][0];
-            uw[(2 * c4 + 1) * C::UPAD + dA] = acc[mt][1];
-            uw[(2 * c4) * C::UPAD + dB] = acc[mt][2];
-            uw[(2 * c4 + 1) * C::UPAD + dB] = acc[mt][3];
-        }
-        named_barrier_sync(1, C::NCW * 32);
-        if (ctid < C::G) {
-            const int g = ctid;
-            float M = -INFINITY;
-            for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, sm_m[w * C::G + g]);
-            float Ls = 0.f;
-            for (int w = 0; w < C::NCW; ++w) {
-                const float mw = sm_m[w * C::G + g];
-                const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-                sm_w[w * C::G + g] = wt;
-                Ls += wt * sm_l[w * C::G + g];
-            }
-            sm_fin[g] = Ls;
-            sm_fin[C::G + g] = M;
-        }
-        named_barrier_sync(1, C::NCW * 32);
+        // one pass per query token of the request (the scratch holds one)
         const bool direct = sg.ns == 1;
         const int split = sg.so + ss;
         const bool split_ok = direct || (split >= 0 && split < p.meta.max_splits);
-        for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
-            const int g = idx / D, d = idx % D;
-            float u = 0.f;
+        const size_t rows = (size_t)p.s_q * p.H_q;  // output rows per request: [s_q][H_q]
 #pragma unroll
-            for (int w = 0; w < C::NCW; ++w) u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
-            const float Ls = sm_fin[g];
-            const float o = (Ls > 0.f) ? (u / Ls) * vscale : 0.f;
-            const size_t hq = (size_t)h * C::G + g;
-            if (direct)
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * p.H_q + hq) * D + d] = __float2bfloat16_rn(o);
-            else if (split_ok)
-                p.meta.o_part[((size_t)split * p.H_q + hq) * D + d] = o;
-        }
-        if (ctid < C::G) {
-            const int g = ctid;
-            const float Ls = sm_fin[g];
-            const float v = (Ls > 0.f) ? (sm_fin[C::G + g] + log2f(Ls)) * kLn2 : -INFINITY;
-            const size_t hq = (size_t)h * C::G + g;
-            if (direct)
-                p.lse[(size_t)sb * p.H_q + hq] = v;
-            else if (split_ok)
-                p.meta.lse_part[(size_t)split * p.H_q + hq] = v;
+        for (int j = 0; j < NQ; ++j) {
+            if (j >= p.s_q) break;
+            if (j > 0) named_barrier_sync(1, C::NCW * 32);  // the previous pass has read the scratch
+            const float lj0 = warp_sum_xor_4_8_16(l0[j]);
+            const float lj1 = warp_sum_xor_4_8_16(l1[j]);
+            if (lane < 4) {
+                sm_m[warp * C::G + 2 * c4] = m0[j];
+                sm_m[warp * C::G + 2 * c4 + 1] = m1[j];
+                sm_l[warp * C::G + 2 * c4] = lj0;
+                sm_l[warp * C::G + 2 * c4 + 1] = lj1;
+            }
+            float *uw = sm_u + (size_t)warp * C::G * C::UPAD;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                // accumulator rows -> head-dim index
+                const int dA = FP8 ? mt * 16 + 2 * r8 : mt * 16 + r8;
+                const int dB = FP8 ? dA + 1 : dA + 8;
+                uw[(2 * c4) * C::UPAD + dA] = acc[mt][j][0];
+                uw[(2 * c4 + 1) * C::UPAD + dA] = acc[mt][j][1];
+                uw[(2 * c4) * C::UPAD + dB] = acc[mt][j][2];
+                uw[(2 * c4 + 1) * C::UPAD + dB] = acc[mt][j][3];
+            }
+            named_barrier_sync(1, C::NCW * 32);
+            if (ctid < C::G) {
+                const int g = ctid;
+                float M = -INFINITY;
+                for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, sm_m[w * C::G + g]);
+                float Ls = 0.f;
+                for (int w = 0; w < C::NCW; ++w) {
+                    const float mw = sm_m[w * C::G + g];
+                    const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                    sm_w[w * C::G + g] = wt;
+                    Ls += wt * sm_l[w * C::G + g];
+                }
+                sm_fin[g] = Ls;
+                sm_fin[C::G + g] = M;
+            }
+            named_barrier_sync(1, C::NCW * 32);
+            const size_t row0 = (size_t)j * p.H_q + (size_t)h * C::G;  // row of head g = row0 + g
+            for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
+                const int g = idx / D, d = idx % D;
+                float u = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::NCW; ++w) u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
+                const float Ls = sm_fin[g];
+                const float o = (Ls > 0.f) ? (u / Ls) * vscale : 0.f;
+                if (direct)
+                    reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * rows + row0 + g) * D + d] =
+                        __float2bfloat16_rn(o);
+                else if (split_ok)
+                    p.meta.o_part[((size_t)split * rows + row0 + g) * D + d] = o;
+            }
+            if (ctid < C::G) {
+                const int g = ctid;
+                const float Ls = sm_fin[g];
+                const float v = (Ls > 0.f) ? (sm_fin[C::G + g] + log2f(Ls)) * kLn2 : -INFINITY;
+                if (direct)
+                    p.lse[(size_t)sb * rows + row0 + g] = v;
+                else if (split_ok)
+                    p.meta.lse_part[(size_t)split * rows + row0 + g] = v;
+            }
         }
         if (named_barrier_or(1, C::NCW * 32, *abort_flag != 0)) break;
     }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NQ>
 static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
                               bool pdl) {
     using C = GqaCfg<D, FP8>;
-    auto kern = gqa_decode_kernel<D, FP8>;
+    auto kern = gqa_decode_kernel<D, FP8, NQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -526,9 +569,17 @@ static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, con
 
 cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p,
                        cudaStream_t stream, bool pdl) {
-    if (!fp8 && D == 64) return launch_one<64, false>(tkv, tv, p, stream, pdl);
-    if (!fp8 && D == 128) return launch_one<128, false>(tkv, tv, p, stream, pdl);
-    if (fp8 && D == 128) return launch_one<128, true>(tkv, tv, p, stream, pdl);
+    if (p.s_q == 1) {
+        if (!fp8 && D == 64) return launch_one<64, false, 1>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 1>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 1>(tkv, tv, p, stream, pdl);
+    } else if (p.s_q == 2) {
+        if (!fp8 && D == 64) return launch_one<64, false, 2>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 2>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 2>(tkv, tv, p, stream, pdl);
+    } else if (p.s_q <= kMaxSqD64 && !fp8 && D == 64) {
+        return launch_one<64, false, kMaxSqD64>(tkv, tv, p, stream, pdl);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -10,6 +10,8 @@ constexpr int kChunk = 64;                 // tokens per scheduling chunk
 constexpr int kTmaElemBytes = 8;           // element size the pool tensor maps are described with
 constexpr int32_t kMetaMagic = 0x44414d31;  // "DAM1"
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr int kMaxSqD64 = 4;               // query tokens per request: bf16 D = 64 kernel
+constexpr int kMaxSqD128 = 2;              // bf16 / e4m3 D = 128 kernels
 
 // sched_meta header words
 enum MetaHeader : int {
@@ -28,6 +30,7 @@ enum MetaHeader : int {
     kHErrorDetail = 12,
     kHKvDtype = 13,
     kHNumSms = 14,
+    kHSq = 15,
     kHeaderWords = 16,
 };
 
@@ -52,8 +55,8 @@ struct MetaView {
     const int32_t *chunk_offset;
     const int32_t *split_offset;
     const int32_t *num_splits;
-    float *lse_part;   // [max_splits][H_q]
-    float *o_part;     // [max_splits][H_q][D_v]
+    float *lse_part;   // [max_splits][s_q * H_q]
+    float *o_part;     // [max_splits][s_q * H_q][D_v]
     float *xchg;       // latent-token kernel only: partial scores swapped between the CTAs of a part
     int32_t max_splits;
 };
@@ -65,19 +68,20 @@ struct SchedParams {
     int32_t *chunk_offset;
     int32_t *split_offset;
     int32_t *num_splits;
-    int32_t B, H_kv, G, splits, num_parts, cpc, max_len, kv_dtype, num_sms;
+    int32_t B, H_kv, G, splits, num_parts, cpc, max_len, kv_dtype, num_sms, s_q;
 };
 
 struct GqaParams {
-    const void *q;                 // bf16 [B][H_q][D]
+    const void *q;                 // bf16 [B][s_q][H_q][D]
     const int32_t *block_table;    // [B][max_pages]
     const int32_t *seqlens;        // [B]
     const float *k_scale;          // [H_kv] (fp8) or null
     const float *v_scale;
     MetaView meta;
-    void *out;                     // bf16 [B][H_q][D]
-    float *lse;                    // [B][H_q]
+    void *out;                     // bf16 [B][s_q][H_q][D]
+    float *lse;                    // [B][s_q][H_q]
     int32_t B, H_kv, G, H_q, max_pages, num_pages, page_size, box_tokens, boxes_per_chunk;
+    int32_t s_q;                   // query tokens per request (draft j sees L - s_q + 1 + j tokens)
     int32_t log2_box_tokens;       // box_tokens is 8, 16, 32 or 64
     int32_t kv_swap;               // 1: the V pool lies below the K pool (its rows come first in a box)
     int32_t kv_combined;           // 1: one 5-D map covers both pools; 0: one 4-D map per pool
@@ -107,9 +111,9 @@ struct MlaParams {
 
 struct CombineParams {
     MetaView meta;
-    void *out;       // bf16 [B][H_q][D_v]
-    float *lse;      // [B][H_q]
-    int32_t B, H_q, D_v, H_kv, G, splits, num_parts;
+    void *out;       // bf16 [B][rows][D_v]
+    float *lse;      // [B][rows]
+    int32_t B, rows, D_v, H_kv, G, splits, num_parts, s_q;   // rows = s_q * H_q per request
 };
 
 struct AppendParams {

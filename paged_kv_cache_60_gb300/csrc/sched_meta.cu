@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
         h[kHErrorDetail] = 0;
         h[kHKvDtype] = p.kv_dtype;
         h[kHNumSms] = p.num_sms;
-        h[15] = 0;
+        h[kHSq] = p.s_q;
     }
 }
 

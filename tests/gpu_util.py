@@ -49,7 +49,7 @@ def make_desc(w, splits=None, num_sms=0):
     return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,
                         max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=s.kv_dtype,
                         splits=s.splits if splits is None else splits, num_sms=num_sms,
-                        softmax_scale=s.softmax_scale)
+                        softmax_scale=s.softmax_scale, s_q=s.s_q)
 
 
 class DeviceWorkload:
@@ -73,10 +73,11 @@ def run(w, splits=None, num_sms=0, dw=None, meta=None, desc=None, out=None, lse=
     if meta is None:
         meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device="cuda")
         da.sched_meta(desc, dw.cache_seqlens, meta, stream=stream)
+    rows = (s.B, s.H_q) if s.s_q == 1 else (s.B, s.s_q, s.H_q)
     if out is None:
-        out = torch.full((s.B, s.H_q, s.D_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+        out = torch.full(rows + (s.D_v,), float("nan"), dtype=torch.bfloat16, device="cuda")
     if lse is None:
-        lse = torch.full((s.B, s.H_q), float("nan"), dtype=torch.float32, device="cuda")
+        lse = torch.full(rows, float("nan"), dtype=torch.float32, device="cuda")
     da.fwd(desc, dw.q, dw.k_pool, dw.v_pool, dw.k_scale, dw.v_scale, dw.block_table, dw.cache_seqlens,
            meta, out, lse, stream=stream)
     return out, lse, meta, desc

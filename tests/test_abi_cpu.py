@@ -126,3 +126,20 @@ def test_append_rejects_bad_arguments_before_launch(lib):
     assert call(dm) == -3                        # the latent token takes no v_new
     assert call(dm, v_new=None, vp=P(0x20000)) == -3
     assert call(_desc(kv_dtype=da.KV_MLA656, H_kv=2, G=128, D_qk=576, D_v=512), v_new=None, vp=None) == -3
+
+
+def test_s_q_limits_and_partial_sizes(lib):
+    n = ctypes.c_size_t(0)
+
+    def rc(**kw):
+        return lib.decode_attn_sched_meta_bytes(ctypes.byref(_desc(**kw)), ctypes.byref(n))
+    assert rc(s_q=0) == 0 and rc(s_q=1) == 0 and rc(s_q=2) == 0
+    assert rc(s_q=3) == -3                                   # D = 128: up to 2 drafts
+    assert rc(D_qk=64, D_v=64, s_q=4) == 0 and rc(D_qk=64, D_v=64, s_q=5) == -3
+    assert rc(kv_dtype=da.KV_FP8, s_q=2) == 0 and rc(kv_dtype=da.KV_FP8, s_q=3) == -3
+    assert rc(s_q=-1) == -2
+    # the split partials hold one row per (draft, query head)
+    o1, o2 = da.meta_offsets(_desc()), da.meta_offsets(_desc(s_q=2))
+    assert o1[:6] == o2[:6]
+    assert (o2[6] - o2[5]) >= 2 * (o1[6] - o1[5]) - 256
+    assert (o2[7] - o2[6]) >= 2 * (o1[7] - o1[6]) - 256

@@ -69,6 +69,20 @@ CONFIGS = [
         splits=0, seed=1004,
         description="B=32 H_q=128 H_kv=1 D_qk=576 D_v=512 P=64 656-byte FP8 tokens, "
                     "L log-uniform [4096,131072]"),
+    # several query tokens per request (a chain of drafts being verified); not
+    # a shape the pages measure: the mixed and FP8 shapes with s_q = 2 and 4
+    WorkloadSpec(
+        name="spec2_gqa_bf16", B=32, H_kv=8, G=8, D_qk=128, D_v=128, page_size=64,
+        length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1005, s_q=2,
+        description="B=32 s_q=2 H_q=64 H_kv=8 D=128 P=64 L~U[1024,8192] auto splits, draft chain of 2"),
+    WorkloadSpec(
+        name="spec2_fp8_gqa", B=64, H_kv=4, G=8, D_qk=128, D_v=128, page_size=32,
+        kv_dtype=KV_FP8, lengths=[32768] * 64, splits=0, seed=1006, s_q=2,
+        description="B=64 s_q=2 H_q=32 H_kv=4 D=128 P=32 L=32768 e4m3 KV, draft chain of 2"),
+    WorkloadSpec(
+        name="spec4_gqa_d64", B=32, H_kv=8, G=8, D_qk=64, D_v=64, page_size=64,
+        length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1007, s_q=4,
+        description="B=32 s_q=4 H_q=64 H_kv=8 D=64 P=64 L~U[1024,8192] auto splits, draft chain of 4"),
 ]
 
 
