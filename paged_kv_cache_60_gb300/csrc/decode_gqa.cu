@@ -51,7 +51,7 @@ namespace da {
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NQ>
 struct GqaCfg {
     static constexpr int G = 8;
     static constexpr int ES = FP8 ? 1 : 2;
@@ -64,8 +64,11 @@ struct GqaCfg {
     // warp then waits on the phases of a stage one after the other, and never
     // on a phase two ahead of the barrier's current one (whose parity would
     // alias an already completed phase).
-    static constexpr int NCW = FP8 ? 10 : (D == 64 ? 5 : 6);
-    static constexpr int NS = FP8 ? 10 : (D == 128 ? 6 : 5);
+    // With several query tokens (NQ > 1) a warp holds NQ times the state and
+    // the kernel runs one CTA per SM: 7 consumer warps keep at most two warps
+    // on each SM sub-partition, so a thread may use up to 255 registers.
+    static constexpr int NCW = NQ > 1 ? (D == 128 && !FP8 ? 6 : 7) : (FP8 ? 10 : (D == 64 ? 5 : 6));
+    static constexpr int NS = NCW == 5 ? 5 : NCW;
     static_assert(NS % NCW == 0, "stage ownership must be fixed per warp");
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int MT = D / 16;
@@ -79,7 +82,7 @@ struct GqaCfg {
     static constexpr int OFF_BAR = (OFF_FIN + 2 * G * 4 + 7) / 8 * 8;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
-    static constexpr int MIN_BLOCKS = (D == 64 && !FP8) ? 2 : 1;
+    static constexpr int MIN_BLOCKS = (D == 64 && !FP8 && NQ == 1) ? 2 : 1;
     static_assert(ROW % 128 == 0, "rows must be whole 128-byte boxes");
     static_assert(!FP8 || NX == 1, "fp8 path expects one 128-byte box per row");
 };
@@ -87,10 +90,10 @@ struct GqaCfg {
 // NQ: query tokens per request the kernel is compiled for (s_q <= NQ; tokens
 // j >= s_q are zero rows that are never written).
 template <int D, bool FP8, int NQ>
-__global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, (NQ == 1) ? GqaCfg<D, FP8>::MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ>::MIN_BLOCKS)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ GqaParams p) {
-    using C = GqaCfg<D, FP8>;
+    using C = GqaCfg<D, FP8, NQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *sm_u = reinterpret_cast<float *>(smem + C::OFF_U);
@@ -550,7 +553,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8>::THREADS, (NQ == 1) ? GqaCfg<D,
 template <int D, bool FP8, int NQ>
 static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
                               bool pdl) {
-    using C = GqaCfg<D, FP8>;
+    using C = GqaCfg<D, FP8, NQ>;
     auto kern = gqa_decode_kernel<D, FP8, NQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
