@@ -6,8 +6,9 @@ benchmark's CPU-baseline leg may import this package; the library under
 
 * ``decode_ref.c``  -- attention by its definition, per (request, KV head,
   head range, token range), plus the split merge; built with gcc + OpenMP.
-  ``attend_multi`` applies it per draft token for several query tokens per
-  request (each draft sees the history and the drafts before it).
+  ``attend_multi`` applies it per query token of the general decode step:
+  several query tokens per request (each draft sees the history and the
+  drafts before it), a sliding window, attention sinks.
 * ``sched_ref.py``  -- the integer split-KV scheduling metadata.
 * ``append_ref.py`` -- appending one new token per request into its page slot,
   with the e4m3 encoder (per-head scales, or the 656-byte latent token).
@@ -142,26 +143,49 @@ def attend(w, heads=None):
 
 
 def attend_multi(w, heads=None):
-    """Several query tokens per request (linear speculative-decoding
-    verification, XQA page, section "投机解码:XQA 的第二个工作负载": the drafts
-    form a chain, so each sees the history and the drafts before it). The
-    request's last s_q tokens are the drafts, already in the cache (L_b counts
-    them); draft j attends over tokens [0, L_b - s_q + 1 + j). w.q is
-    [B, s_q, H_q, D_qk]. Returns out [B, s_q, H_q, D_v] and lse [B, s_q, H_q]
-    (float64; NaN where not computed; lse -inf for a draft that sees nothing)."""
+    """The general decode step: s_q query tokens per request, an optional
+    sliding window and optional attention sinks. Returns out [B, s_q, H_q, D_v]
+    and lse [B, s_q, H_q] (float64; NaN where not computed).
+
+    * Drafts (s_q > 1; linear speculative-decoding verification, XQA page,
+      section "投机解码:XQA 的第二个工作负载": the drafts form a chain, so each
+      sees the history and the drafts before it): the request's last s_q
+      tokens are the drafts, already in the cache (L_b counts them); draft j
+      is at position L_b - s_q + j and sees the tokens up to it. w.q is
+      [B, s_q, H_q, D_qk] (or [B, H_q, D_qk] when s_q = 1).
+    * Sliding window W > 0 (XQA page, section "分页 KV:页号怎么变成 TMA 坐标"):
+      a query token sees only the last W tokens up to and including itself.
+    * Sinks (XQA page, section "一个容易漏掉的细节:attention sink"): one logit
+      per query head, w.sinks[hq], in the units of the scores sigma q.k, that
+      joins the softmax denominator and carries no value:
+      lse = ln(e^sink + sum_t e^{s_t}), out = sum_t e^{s_t - lse} v_t. A row
+      that sees no token has out = 0 and lse = sink (-inf without sinks).
+    """
     s = w.spec
     sq = s.s_q
+    W = s.window
     if heads is None:
         heads = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
     out = torch.full((s.B, sq, s.H_q, s.D_v), float("nan"), dtype=torch.float64)
     lse = torch.full((s.B, sq, s.H_q), float("nan"), dtype=torch.float64)
     q = w.q.view(s.B, sq, s.H_q, s.D_qk)
     for j in range(sq):
-        units = [(b, h, 0, s.G, 0, max(0, w.lengths[b] - sq + 1 + j)) for (b, h) in heads]
+        units = []
+        for (b, h) in heads:
+            hi = max(0, w.lengths[b] - sq + 1 + j)
+            lo = max(0, hi - W) if W > 0 else 0
+            units.append((b, h, 0, s.G, lo, hi))
         o, l = attend_units(w, units, q64=q[:, j].to(torch.float64).contiguous())
         for i, (b, h) in enumerate(heads):
             out[b, j, h * s.G:(h + 1) * s.G] = o[i]
             lse[b, j, h * s.G:(h + 1) * s.G] = l[i]
+    if getattr(w, "sinks", None) is not None:
+        sink = w.sinks.to(torch.float64).view(1, 1, s.H_q).expand_as(lse)
+        done = ~torch.isnan(lse)
+        tot = torch.logaddexp(lse, sink)
+        fac = torch.where(torch.isneginf(lse), torch.zeros_like(lse), torch.exp(lse - tot))
+        out = torch.where(done.unsqueeze(-1), out * fac.unsqueeze(-1), out)
+        lse = torch.where(done, tot, lse)
     return out, lse
 
 
@@ -181,7 +205,7 @@ def attend_split_combine(w, ref: SchedRef):
     """Oracle split-then-combine over the token ranges that ``ref`` assigns:
     every split computed on its own, then merged. Returns out, lse like attend()."""
     s = w.spec
-    ranges = split_token_ranges(ref, w.lengths)
+    ranges = split_token_ranges(ref, w.lengths, w.spec.window, w.spec.s_q)
     units, index = [], []
     for b in range(s.B):
         for h in range(s.H_kv):

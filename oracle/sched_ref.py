@@ -4,7 +4,12 @@ TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
 benchmark's CPU baseline, never by the library.
 
 Work is counted in chunks of C = 64 tokens; request b has
-n_b = ceil(L_b / C) chunks.
+n_b = ceil(L_b / C) - f_b chunks, its chunks f_b .. ceil(L_b / C) - 1. f_b = 0
+unless a sliding window of W tokens is set: then the first query token (of s_q
+per request) sees tokens from start_b = max(0, L_b - s_q + 1 - W) on, and the
+chunks before the one holding start_b are never read, f_b = floor(start_b / C)
+(XQA page, section "分页 KV:页号怎么变成 TMA 坐标": with a sliding window the
+leading pages are skipped).
 
 * Fixed mode (splits = S > 0) follows the split range of FlashAttention's
   block.h (FlashAttention tiling page, section 5.3 "Split 在 block.h 中的实现"):
@@ -34,6 +39,15 @@ def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
+def window_start(L: int, window: int = 0, s_q: int = 1) -> int:
+    """First token any query token of the request sees."""
+    return max(0, L - s_q + 1 - window) if window > 0 else 0
+
+
+def first_chunk(L: int, window: int = 0, s_q: int = 1) -> int:
+    return window_start(max(0, L), window, s_q) // CHUNK
+
+
 def auto_num_parts(num_sms: int, H_kv: int, cpc: int) -> int:
     return max(1, num_sms // (H_kv * cpc))
 
@@ -50,9 +64,10 @@ class SchedRef:
     parts: List[Tuple[int, int, int, int]]
 
 
-def sched_ref(seqlens: List[int], H_kv: int, splits: int, num_sms: int, cpc: int = 1) -> SchedRef:
+def sched_ref(seqlens: List[int], H_kv: int, splits: int, num_sms: int, cpc: int = 1, window: int = 0,
+              s_q: int = 1) -> SchedRef:
     B = len(seqlens)
-    n = [ceil_div(max(0, L), CHUNK) for L in seqlens]
+    n = [ceil_div(max(0, L), CHUNK) - first_chunk(L, window, s_q) for L in seqlens]
     chunk_offset = [0]
     for x in n:
         chunk_offset.append(chunk_offset[-1] + x)
@@ -120,13 +135,17 @@ def part_segments(ref: SchedRef, p: int):
     return out
 
 
-def split_token_ranges(ref: SchedRef, seqlens: List[int]):
-    """For every request, the token range [t0, t1) of each of its splits, in split order."""
+def split_token_ranges(ref: SchedRef, seqlens: List[int], window: int = 0, s_q: int = 1):
+    """For every request, the token range [t0, t1) of each of its splits, in
+    split order (local chunk lc is the request's chunk f_b + lc; the first
+    split starts at the window start)."""
     B = len(seqlens)
     ranges = [[None] * ref.num_splits[b] for b in range(B)]
     for p in range(ref.num_parts):
         for (b, s, lc0, lc1) in part_segments(ref, p):
-            t0 = min(lc0 * CHUNK, seqlens[b])
-            t1 = min(lc1 * CHUNK, seqlens[b])
+            L = seqlens[b]
+            f = first_chunk(L, window, s_q)
+            t0 = max(window_start(L, window, s_q), min((f + lc0) * CHUNK, L))
+            t1 = max(t0, min((f + lc1) * CHUNK, L))
             ranges[b][s] = (t0, t1)
     return ranges

@@ -39,35 +39,88 @@ def _kv_rows(w, b, h):
     return torch.stack(ks), torch.stack(vs)
 
 
-@pytest.mark.parametrize("kv_dtype", [KV_BF16, KV_FP8])
-def test_masked_matrix_formulation(oracle_lib, kv_dtype):
-    spec = _spec(kv_dtype=kv_dtype)
+@pytest.mark.parametrize("kv_dtype,s_q,window,sinks", [
+    (KV_BF16, 3, 0, False), (KV_FP8, 3, 0, False), (KV_BF16, 1, 5, False), (KV_BF16, 3, 4, True),
+    (KV_FP8, 2, 7, True), (KV_BF16, 1, 0, True),
+])
+def test_masked_matrix_formulation(oracle_lib, kv_dtype, s_q, window, sinks):
+    """Scores as one matrix per (request, query head): rows = query tokens,
+    columns = [sink] + tokens, invisible tokens set to -inf; torch's softmax
+    and logsumexp give the weights and lse; the sink column carries no value."""
+    spec = _spec(kv_dtype=kv_dtype, s_q=s_q, window=window, sinks=sinks)
     w = make_workload(spec, poison=False)
     out, lse = oracle.attend_multi(w)
     s = spec
     sigma = w.softmax_scale
-    q = w.q.double()
+    q = w.q.double().view(s.B, s.s_q, s.H_q, s.D_qk)
     for b in range(s.B):
         L = w.lengths[b]
         for h in range(s.H_kv):
             K, V = _kv_rows(w, b, h)
-            # mask[j, t]: draft j (at position L - s_q + j) sees token t <= its own position
+            # visible[j, t]: query token j sits at position L - s_q + j and sees
+            # token t at or before it, and within the last `window` tokens
             t = torch.arange(L).view(1, L)
-            j = torch.arange(s.s_q).view(s.s_q, 1)
-            visible = t <= (L - s.s_q + j)
+            pos = (L - s.s_q + torch.arange(s.s_q)).view(s.s_q, 1)
+            visible = t <= pos
+            if window:
+                visible &= t > pos - window
             for g in range(s.G):
                 hq = h * s.G + g
                 S = sigma * (q[b, :, hq] @ K.T)                     # [s_q, L]
                 S = S.masked_fill(~visible, float("-inf"))
-                ref_lse = torch.logsumexp(S, dim=1) if L else torch.full((s.s_q,), float("-inf"), dtype=torch.float64)
+                sink = float(w.sinks[hq]) if sinks else float("-inf")
+                S = torch.cat([torch.full((s.s_q, 1), sink, dtype=torch.float64), S], dim=1)
+                ref_lse = torch.logsumexp(S, dim=1)
                 for jj in range(s.s_q):
                     if torch.isinf(ref_lse[jj]):
                         assert lse[b, jj, hq] == float("-inf")
                         assert torch.all(out[b, jj, hq] == 0)
                         continue
-                    p = torch.softmax(S[jj], dim=0)
+                    p = torch.softmax(S[jj], dim=0)[1:]
                     assert abs(float(lse[b, jj, hq] - ref_lse[jj])) < 1e-12
-                    assert torch.allclose(out[b, jj, hq], p @ V, rtol=0, atol=1e-12)
+                    ref_o = p @ V if L else torch.zeros(s.D_v, dtype=torch.float64)
+                    assert torch.allclose(out[b, jj, hq], ref_o, rtol=0, atol=1e-12)
+
+
+def test_window_covering_everything_and_window_one(oracle_lib):
+    spec = _spec(s_q=2)
+    w = make_workload(spec, poison=False)
+    out0, lse0 = oracle.attend_multi(w)
+    wide = dataclasses.replace(w, spec=spec.with_(window=10 ** 6))
+    out1, lse1 = oracle.attend_multi(wide)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    # a window of one token: each query token sees only itself
+    one = dataclasses.replace(w, spec=spec.with_(window=1))
+    out, lse = oracle.attend_multi(one)
+    P = spec.page_size
+    for b, L in enumerate(w.lengths):
+        for j in range(2):
+            t = L - 2 + j
+            if t < 0:
+                assert torch.all(torch.isneginf(lse[b, j]))
+                continue
+            page = int(w.block_table[b, t // P])
+            for h in range(spec.H_kv):
+                v = w.v_pool[page, t % P, h].double()
+                k = w.k_pool[page, t % P, h].double()
+                for g in range(spec.G):
+                    hq = h * spec.G + g
+                    assert torch.equal(out[b, j, hq], v)
+                    s_t = w.softmax_scale * float(w.q[b, j, hq].double() @ k)
+                    assert abs(float(lse[b, j, hq]) - s_t) < 1e-12
+
+
+def test_sinks_limits(oracle_lib):
+    """A sink of -inf is no sink; a very large sink takes all the weight."""
+    spec = _spec(s_q=1, sinks=True)
+    w = make_workload(spec, poison=False)
+    plain = dataclasses.replace(w, sinks=None)
+    out0, lse0 = oracle.attend_multi(plain)
+    out1, lse1 = oracle.attend_multi(dataclasses.replace(w, sinks=torch.full_like(w.sinks, float("-inf"))))
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    out2, lse2 = oracle.attend_multi(dataclasses.replace(w, sinks=torch.full_like(w.sinks, 80.0)))
+    assert torch.all(out2.abs() < 1e-25)
+    assert torch.allclose(lse2, torch.full_like(lse2, 80.0), rtol=0, atol=1e-12)
 
 
 def test_last_draft_is_single_token_decode(oracle_lib):
@@ -94,3 +147,17 @@ def test_drafts_do_not_see_later_tokens(oracle_lib):
     assert torch.equal(out0[:, :-1], out1[:, :-1]) and torch.equal(lse0[:, :-1], lse1[:, :-1])
     assert not torch.equal(out0[:, -1], out1[:, -1])
     assert not torch.equal(lse0[:, -1], lse1[:, -1])
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_windowed_split_and_combine_equals_unsplit(oracle_lib, splits):
+    from oracle.sched_ref import sched_ref
+    spec = _spec(s_q=1, window=70, lengths=[1, 64, 65, 200, 333, 0], splits=splits)
+    w = make_workload(spec, poison=False)
+    ref = sched_ref(w.lengths, spec.H_kv, splits, num_sms=16, window=70)
+    o, l = oracle.attend_split_combine(w, ref)
+    out, lse = oracle.attend_multi(w)
+    assert torch.allclose(o, out[:, 0], rtol=0, atol=1e-12)
+    fin = ~torch.isneginf(lse[:, 0])
+    assert torch.equal(torch.isneginf(l), ~fin)
+    assert torch.allclose(l[fin], lse[:, 0][fin], rtol=0, atol=1e-12)

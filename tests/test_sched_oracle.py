@@ -107,3 +107,33 @@ def test_fixed_mode_tiles_each_request(seed):
             assert t0 == pos and t1 >= t0 and (t1 - t0) <= per * CHUNK
             pos = t1
         assert pos == L
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_window_chunks_are_exactly_the_read_ones(seed):
+    """With a sliding window, a request's chunks are exactly the 64-token
+    chunks that hold a token some query token sees (brute force over tokens),
+    and the splits' token ranges tile [first visible token, L)."""
+    rng = random.Random(500 + seed)
+    B = rng.randint(1, 9)
+    s_q = rng.choice([1, 2, 4])
+    W = rng.choice([1, 5, 64, 100, 1000])
+    lengths = [rng.choice([0, 1, 3, 63, 64, 65, 200, rng.randint(0, 3000)]) for _ in range(B)]
+    splits = rng.choice([0, 1, 3])
+    ref = sched_ref(lengths, H_kv=2, splits=splits, num_sms=rng.choice([16, 152]), window=W, s_q=s_q)
+    for b, L in enumerate(lengths):
+        seen = set()
+        for j in range(s_q):
+            pos = L - s_q + j
+            for t in range(max(0, pos - W + 1), pos + 1):
+                seen.add(t // CHUNK)
+        n = ref.chunk_offset[b + 1] - ref.chunk_offset[b]
+        if not seen:
+            assert n == 0
+            continue
+        assert n == max(seen) - min(seen) + 1 == len(seen)
+    ranges = split_token_ranges(ref, lengths, window=W, s_q=s_q)
+    for b, L in enumerate(lengths):
+        start = max(0, L - s_q + 1 - W)
+        toks = [t for (t0, t1) in ranges[b] for t in range(t0, t1)]
+        assert toks == list(range(start, L)) if L > 0 else toks == []

@@ -36,6 +36,8 @@ class WorkloadSpec:
     softmax_scale: float = 0.0          # 0 = 1/sqrt(D_qk)
     seed: int = 0
     s_q: int = 1                        # query tokens per request (draft tokens of a linear chain)
+    window: int = 0                     # sliding window in tokens (0: none)
+    sinks: bool = False                 # one attention-sink logit per query head
     description: str = field(default="", compare=False)
 
     @property

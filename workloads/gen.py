@@ -59,6 +59,7 @@ class Workload:
     v_scale: Optional[torch.Tensor]
     block_table: torch.Tensor       # int32 [B, max_pages_per_seq]
     cache_seqlens: torch.Tensor     # int32 [B]
+    sinks: Optional[torch.Tensor] = None  # fp32 [H_q] attention-sink logits, or None
 
     @property
     def softmax_scale(self) -> float:
@@ -68,7 +69,10 @@ class Workload:
     def kv_bytes(self) -> int:
         """Bytes of K and V that a decode pass must read once per KV head."""
         s = self.spec
-        tok = int(sum(self.lengths))
+        if s.window > 0:   # tokens before the first query token's window are not read
+            tok = int(sum(L - max(0, L - s.s_q + 1 - s.window) for L in self.lengths if L > 0))
+        else:
+            tok = int(sum(self.lengths))
         if s.kv_dtype == KV_MLA656:
             return tok * s.H_kv * MLA_ROW_BYTES
         es = {KV_BF16: 2, KV_FP8: 1, KV_F64: 8}[s.kv_dtype]
@@ -217,9 +221,14 @@ def make_workload(spec: WorkloadSpec, lengths: Optional[List[int]] = None,
     else:
         raise ValueError(spec.kv_dtype)
 
+    sinks = None
+    if spec.sinks:
+        # per query head, around ln 64: a sink worth tens of tokens of weight
+        gs = torch.Generator().manual_seed(spec.seed + 17)
+        sinks = (torch.randn(H_q, generator=gs) * 2.0 + math.log(64.0)).float()
     return Workload(spec=spec, lengths=lengths, num_pages=num_pages, max_pages_per_seq=maxp,
                     q=q, k_pool=k_pool, v_pool=v_pool, k_scale=k_scale, v_scale=v_scale,
-                    block_table=bt, cache_seqlens=torch.tensor(lengths, dtype=torch.int32))
+                    block_table=bt, cache_seqlens=torch.tensor(lengths, dtype=torch.int32), sinks=sinks)
 
 
 def place_logical(w: Workload, b: int, t: int, k_row=None, v_row=None):
@@ -251,7 +260,7 @@ def repermute_pages(w: Workload, seed: int) -> Workload:
                     max_pages_per_seq=w.max_pages_per_seq, q=w.q.clone(),
                     k_pool=move(w.k_pool), v_pool=move(w.v_pool),
                     k_scale=w.k_scale, v_scale=w.v_scale,
-                    block_table=bt.to(torch.int32), cache_seqlens=w.cache_seqlens.clone())
+                    block_table=bt.to(torch.int32), cache_seqlens=w.cache_seqlens.clone(), sinks=w.sinks)
 
 
 def make_append_batch(w: Workload, seed: int):
