@@ -169,7 +169,7 @@ def make_desc(da, w):
     s = w.spec
     return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,
                         max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=s.kv_dtype,
-                        splits=s.splits, softmax_scale=s.softmax_scale, s_q=s.s_q)
+                        splits=s.splits, softmax_scale=s.softmax_scale, s_q=s.s_q, window=s.window)
 
 
 class DevCopy:
@@ -182,6 +182,7 @@ class DevCopy:
         self.v_scale = w.v_scale.to(dev) if w.v_scale is not None else None
         self.block_table = w.block_table.to(dev)
         self.cache_seqlens = w.cache_seqlens.to(dev)
+        self.sinks = w.sinks.to(dev) if w.sinks is not None else None
         s = w.spec
         self.meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device=dev)
         self.out = torch.empty(s.B, s.s_q * s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
@@ -202,7 +203,7 @@ class DevCopy:
 
     def fwd(self, da, desc, stream, **kw):
         da.fwd(desc, self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale, self.block_table,
-               self.cache_seqlens, self.meta, self.out, self.lse, stream=stream, **kw)
+               self.cache_seqlens, self.meta, self.out, self.lse, stream=stream, sinks=self.sinks, **kw)
 
     def step(self, da, desc, stream, **kw):
         self.sched(da, desc, stream)
@@ -427,7 +428,7 @@ def run_ours(args, rank, world, local):
     e2e = None
     with torch.cuda.stream(stream):
         host = {k: getattr(devs[0], k).cpu().pin_memory() for k in
-                ("q", "k_pool", "v_pool", "k_scale", "v_scale", "block_table", "cache_seqlens")
+                ("q", "k_pool", "v_pool", "k_scale", "v_scale", "block_table", "cache_seqlens", "sinks")
                 if getattr(devs[0], k) is not None}
         h_out = torch.empty_like(devs[0].out, device="cpu").pin_memory()
         h_lse = torch.empty_like(devs[0].lse, device="cpu").pin_memory()
@@ -472,6 +473,7 @@ def run_ours(args, rank, world, local):
                 spec.kv_dtype, "fp8-e4m3 656-byte kv dequantised to bf16 / bf16 q,out"),
             "data": "synthetic",
             "config": {"workload": args.workload, "desc": spec.description, "B": spec.B, "s_q": spec.s_q,
+                       "window": spec.window, "sinks": spec.sinks,
                        "H_q": spec.H_q,
                        "H_kv": spec.H_kv, "D_qk": spec.D_qk, "D_v": spec.D_v, "page_size": spec.page_size,
                        "splits": spec.splits, "kv_bytes_per_call": kv_bytes,

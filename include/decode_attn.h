@@ -77,6 +77,7 @@ typedef struct {
     int32_t num_sms;           /* 0: query the current device */
     float softmax_scale;       /* sigma; 0: 1/sqrt(D_qk) */
     int32_t s_q;               /* query tokens per request (0 means 1); see decode_attn_fwd */
+    int32_t window;            /* sliding window W in tokens (0: none); see decode_attn_fwd */
 } da_desc;
 
 /* Return codes. */
@@ -110,9 +111,9 @@ int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
 /*
  * Byte offsets inside sched_meta, for inspection and tests. offs[0..7] =
  * header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part,
- * total size. Header (16 int32): magic, B, H_kv, G, splits, num_parts, cpc,
+ * total size. Header (32 int32): magic, B, H_kv, G, splits, num_parts, cpc,
  * chunk (64), total_chunks, total_splits, per, error word, error detail,
- * kv_dtype, num_sms, s_q. parts: num_parts records of 8 int32
+ * kv_dtype, num_sms, s_q, window, then zeros. parts: num_parts records of 8 int32
  * {b0, s0, c0, c1, co0, L0, so0, ns0}: first request, its split index there,
  * global chunk interval [c0, c1), then chunk_offset[b0], min(L_b0,
  * max_pages_per_seq*page_size), split_offset[b0], num_splits[b0] (all 0 when
@@ -132,6 +133,11 @@ int decode_attn_num_parts(const da_desc *desc, int32_t *num_parts);
  *     (FlashAttention tiling page, section 5.3, block.h split range);
  *   splits = 0: all chunks of all requests are cut into
  *     num_parts = floor(num_sms / (H_kv * cpc)) equal intervals, one per part.
+ * With a sliding window (desc->window = W > 0) a request's chunks start at the
+ * one holding token max(0, L_b - s_q + 1 - W), the first its first query token
+ * sees: the pages before it are never read (XQA page, section
+ * "分页 KV:页号怎么变成 TMA 坐标"), and their block_table entries may hold
+ * anything.
  * cache_seqlens: device int32 [B]. sched_meta: device, caller-owned, at least
  * decode_attn_sched_meta_bytes. Launches one small kernel on `stream`; the
  * result may be reused by any number of decode_attn_fwd calls while
@@ -154,6 +160,15 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
  * the 656-byte format takes s_q = 1. The rows of q, out and lse below are
  * then [B][s_q][H_kv*G]; the scheduling metadata must be built with the same s_q.
  *
+ * Sliding window (desc->window = W > 0; XQA page, section
+ * "分页 KV:页号怎么变成 TMA 坐标"): a query token at position p sees only the
+ * tokens (p - W, p]. Attention sinks (da_launch_opts.sinks; XQA page, section
+ * "一个容易漏掉的细节:attention sink"): one fp32 logit per query head, in the
+ * units of sigma * q.k, that joins each row's softmax denominator and carries
+ * no value: lse = ln(e^sink + sum_t e^{s_t}), out = sum_t e^{s_t - lse} v_t;
+ * a row that sees no token gets out = 0 and lse = sink. Both are for the
+ * bf16 and e4m3 formats (DA_ERR_UNSUPPORTED with the 656-byte format).
+ *
  *   q:            bf16 [B][H_kv*G][D_qk], query head h*G+g belongs to KV head h
  *   k_pool/v_pool: see da_kv_dtype
  *   k_scale/v_scale: fp32 [H_kv] for DA_KV_FP8_PER_TENSOR, else ignored
@@ -174,9 +189,10 @@ typedef struct {
     int32_t use_pdl;          /* 1 (default behaviour of decode_attn_fwd): PDL-chain the kernels */
     cudaEvent_t main_begin;   /* if not NULL: recorded on `stream` just before the split-KV kernel */
     cudaEvent_t main_end;     /* if not NULL: recorded just after it (before the combine kernel) */
+    const float *sinks;       /* if not NULL: device fp32 [H_kv*G] attention-sink logits (see decode_attn_fwd) */
 } da_launch_opts;
 
-/* decode_attn_fwd with launch options (opts may be NULL). */
+/* decode_attn_fwd with launch options and optional inputs (opts may be NULL). */
 int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
                        const float *k_scale, const float *v_scale, const int32_t *block_table,
                        const int32_t *cache_seqlens, void *sched_meta, size_t sched_meta_bytes,

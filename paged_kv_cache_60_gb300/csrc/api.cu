@@ -48,6 +48,7 @@ int check_desc(const da_desc *d) {
     if (d->num_sms < 0) return DA_ERR_DIMS;
     if (!(d->softmax_scale >= 0.f) || std::isinf(d->softmax_scale)) return DA_ERR_DIMS;
     if (d->s_q < 0 || d->s_q > 64) return DA_ERR_DIMS;
+    if (d->window < 0) return DA_ERR_DIMS;
     const int sq = sq_of(d);
     const int P = d->page_size;
     const bool page_ok = (P == 8 || P == 16 || P == 32 || (P % 64) == 0);
@@ -63,7 +64,7 @@ int check_desc(const da_desc *d) {
             break;
         case DA_KV_FP8_MLA656:
             if (d->H_kv != 1 || d->D_qk != 576 || d->D_v != 512 || d->G != 128) return DA_ERR_UNSUPPORTED;
-            if (sq != 1) return DA_ERR_UNSUPPORTED;
+            if (sq != 1 || d->window != 0) return DA_ERR_UNSUPPORTED;
             if (!mla_kernel_available()) return DA_ERR_UNSUPPORTED;
             break;
         default:
@@ -269,6 +270,7 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens, vo
     p.kv_dtype = desc->kv_dtype;
     p.num_sms = nsm;
     p.s_q = sq_of(desc);
+    p.window = desc->window;
     if (launch_sched_meta(p, stream, true) != cudaSuccess) return DA_ERR_CUDA;
     return DA_OK;
 }
@@ -293,6 +295,9 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
             return DA_ERR_ALIGN;
     }
     if (sched_meta_bytes < L.total) return DA_ERR_META_SIZE;
+    const float *sinks = opts ? opts->sinks : nullptr;
+    if (sinks && mla) return DA_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(sinks) & 3u) return DA_ERR_ALIGN;
     const bool pdl = opts ? opts->use_pdl != 0 : true;
     const float sigma = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->D_qk);
     const MetaView mv = meta_view(sched_meta, L);
@@ -333,6 +338,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.G = desc->G;
         p.H_q = H_q;
         p.s_q = sq_of(desc);
+        p.window = desc->window;
+        p.sinks = sinks;
         p.max_pages = desc->max_pages_per_seq;
         p.num_pages = desc->num_pages;
         p.page_size = P;
@@ -381,6 +388,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
     c.B = desc->B;
     c.rows = H_q * sq_of(desc);
     c.s_q = sq_of(desc);
+    c.window = desc->window;
+    c.sinks = sinks;
     c.D_v = desc->D_v;
     c.H_kv = desc->H_kv;
     c.G = desc->G;

@@ -29,8 +29,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     const int32_t *hd = p.meta.header;
     const int ns = p.meta.num_splits[b];
     const int so = p.meta.split_offset[b];
-    if (!(hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv && hd[kHG] == p.G &&
-          hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts && hd[kHSq] == p.s_q))
+    if (!meta_header_ok(load_meta_header(hd), p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q, p.window))
         return;  // the split-KV kernel has flagged the mismatch
     if (hq >= p.rows) return;
     if (ns == 1) return;  // written directly by the split-KV kernel
@@ -80,6 +79,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
                 }
             }
         }
+    }
+    if (p.sinks != nullptr) {
+        // the attention sink joins the denominator once, after the splits are
+        // merged (XQA page, section "一个容易漏掉的细节:attention sink")
+        const float tot = log_add_exp(lse_v, p.sinks[hq % (p.rows / p.s_q)]);
+        const float fac = (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
+#pragma unroll
+        for (int k = 0; k < PER_LANE; ++k) acc[k] *= fac;
+        lse_v = tot;
     }
     if constexpr (PER_LANE == 2) {
         reinterpret_cast<__nv_bfloat162 *>(op)[lane] = __floats2bfloat162_rn(acc[0], acc[1]);

@@ -79,7 +79,7 @@ struct GqaCfg {
     static constexpr int OFF_L = OFF_M + NCW * G * 4;
     static constexpr int OFF_W = OFF_L + NCW * G * 4;
     static constexpr int OFF_FIN = OFF_W + NCW * G * 4;
-    static constexpr int OFF_BAR = (OFF_FIN + 2 * G * 4 + 7) / 8 * 8;
+    static constexpr int OFF_BAR = (OFF_FIN + 4 * G * 4 + 7) / 8 * 8;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
     static constexpr int MIN_BLOCKS = (D == 64 && !FP8 && NQ == 1) ? 2 : 1;
@@ -88,8 +88,9 @@ struct GqaCfg {
 };
 
 // NQ: query tokens per request the kernel is compiled for (s_q <= NQ; tokens
-// j >= s_q are zero rows that are never written).
-template <int D, bool FP8, int NQ>
+// j >= s_q are zero rows that are never written). WIN: built with sliding
+// window support (without it, p.window must be 0).
+template <int D, bool FP8, int NQ, bool WIN>
 __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ>::MIN_BLOCKS)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ GqaParams p) {
@@ -133,9 +134,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
     const int4 rec1 = p.meta.parts[2 * part + 1];
     {
         const int32_t *hd = p.meta.header;
-        const bool ok = hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == p.H_kv &&
-                        hd[kHG] == p.G && hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts &&
-                        hd[kHSq] == p.s_q && (int)gridDim.x == p.num_parts;
+        const bool ok = meta_header_ok(load_meta_header(hd), p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q,
+                                       p.window) &
+                        ((int)gridDim.x == p.num_parts);
         if (!ok) {
             if (threadIdx.x == 0) atomicOr(&p.meta.header[kHError], DA_DEV_META_MISMATCH);
             return;
@@ -165,10 +166,14 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
             const int lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
             if (lc0 == lc1) continue;
             const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
-            // page id of this lane's box in chunk lc, or -2 when the box lies past the sequence
+            // local chunk lc is the request's chunk fc + lc (fc > 0 only with a sliding window)
+            const int start = WIN ? window_start(L, p.s_q, p.window) : 0;
+            const int fc = start / kChunk;
+            // page id of this lane's box in chunk lc, or -2 when the box lies past
+            // the sequence or wholly before the window (its page is not read)
             auto id_of = [&](int lc) -> int {
-                const int tok = lc * kChunk + lane * bt;
-                return (lc < lc1 && tok < L) ? bt_row[tok / P] : -2;
+                const int tok = (fc + lc) * kChunk + lane * bt;
+                return (lc < lc1 && tok < L && tok + bt > start) ? bt_row[tok / P] : -2;
             };
             int ring[4];
 #pragma unroll
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
                     }
 #ifdef DA_PAGE_TRACE
                     if (p.page_trace && i < p.page_trace_cap) {
-                        const int tok = (lc + k) * kChunk + lane * bt;
+                        const int tok = (fc + lc + k) * kChunk + lane * bt;
                         const size_t unit = (size_t)blockIdx.x * gridDim.y + blockIdx.y;
                         p.page_trace[(unit * p.page_trace_cap + i) * nb + lane] =
                             pg == -2 ? -2 : pg * P + ((P > kChunk) ? (tok % P) : 0);
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
 #endif
                     mbar_arrive_expect_tx(&full[stage], pg == -2 ? 0u : box_bytes);
                     if (pg != -2) {
-                        const int tok = (lc + k) * kChunk + lane * bt;
+                        const int tok = (fc + lc + k) * kChunk + lane * bt;
                         const int in_page = (P > kChunk) ? (tok % P) : 0;
                         uint8_t *st = smem + (size_t)stage * C::STAGE + lane * box_bytes;
                         if (p.kv_combined) {
@@ -289,8 +294,11 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
                 }
             }
         }
-        // draft token j sees the first L - s_q + 1 + j tokens
+        // draft token j sees the first L - s_q + 1 + j tokens (the last `window`
+        // of them with a sliding window); local chunk lc is the request's chunk fc + lc
         const int L_first = L - p.s_q + 1;
+        const int start = WIN ? window_start(L, p.s_q, p.window) : 0;
+        const int fc = start / kChunk;
         float m0[NQ], m1[NQ], l0[NQ], l1[NQ];
         float acc[C::MT][NQ][4];
 #pragma unroll
@@ -322,19 +330,25 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
                 }
                 break;
             }
-            const int nvalid = L - lc * kChunk;  // >= 1: tokens of this chunk the last draft token sees
+            const int cbase = (fc + lc) * kChunk;  // first token of this chunk
+            const int nvalid = L - cbase;          // >= 1: tokens of this chunk the last draft token sees
+            const int nskip = WIN ? start - cbase : 0;  // > 0: rows before the window (first chunk only)
             uint8_t *stage_ptr = smem + (size_t)stage * C::STAGE;
             const uint32_t s_base = smem_u32(stage_ptr);
             const bool tail = nvalid < kChunk;
-            if (tail) {
-                // rows past the sequence end hold stale or poisoned bytes: zero them
-                // in V so that 0-weight tokens contribute exactly 0 (S is masked below)
-                const int nrow = kChunk - nvalid;
-                for (int e = lane; e < nrow * C::NX * 8; e += 32) {
-                    const int tok = nvalid + e / (C::NX * 8), c16 = e % (C::NX * 8);
-                    uint4 *vr = reinterpret_cast<uint4 *>(stage_ptr + row_of(tok) + v_half);
-                    vr[c16] = make_uint4(0u, 0u, 0u, 0u);
-                }
+            if (tail || nskip > 0) {
+                // rows past the sequence end or before the window hold stale or
+                // poisoned bytes (or were not loaded): zero them in V so that
+                // 0-weight tokens contribute exactly 0 (S is masked below)
+                auto zero_v = [&](int a0, int a1) {
+                    for (int e = lane; e < (a1 - a0) * C::NX * 8; e += 32) {
+                        const int tok = a0 + e / (C::NX * 8), c16 = e % (C::NX * 8);
+                        uint4 *vr = reinterpret_cast<uint4 *>(stage_ptr + row_of(tok) + v_half);
+                        vr[c16] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                };
+                if (nskip > 0) zero_v(0, nskip);     // nskip <= nvalid: the ranges do not overlap
+                if (tail) zero_v(nvalid, kChunk);
                 __syncwarp();
             }
             // ---- S^T = K Q^T for four independent 16-token tiles
@@ -385,12 +399,15 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
             uint32_t pb[4][NQ][2];
 #pragma unroll
             for (int j = 0; j < NQ; ++j) {
-                const int nv = (NQ == 1) ? nvalid : L_first + j - lc * kChunk;
+                const int nv = (NQ == 1) ? nvalid : L_first + j - cbase;
+                // with a window, draft j sees tokens from L_first + j - window on
+                const int lv = (WIN && p.window > 0) ? L_first + j - p.window - cbase : -1;
                 float sv[4][4];
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const bool va = 16 * t + r8 < nv, vb = 16 * t + r8 + 8 < nv;
+                    const int ra = 16 * t + r8, rb = ra + 8;
+                    const bool va = ra < nv && ra >= lv, vb = rb < nv && rb >= lv;
                     sv[t][0] = va ? sacc[t][j][0] * sl2 : -INFINITY;
                     sv[t][1] = va ? sacc[t][j][1] * sl2 : -INFINITY;
                     sv[t][2] = vb ? sacc[t][j][2] * sl2 : -INFINITY;
@@ -472,7 +489,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
                     }
                 }
             }
-            if (tail) fence_proxy_async_smem();  // generic writes above, TMA writes next
+            if (tail || nskip > 0) fence_proxy_async_smem();  // generic writes above, TMA writes next
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
@@ -519,7 +536,16 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
                     Ls += wt * sm_l[w * C::G + g];
                 }
                 sm_fin[g] = Ls;
-                sm_fin[C::G + g] = M;
+                // lse over the tokens; a request with a single split gets its
+                // attention sink here (the combine adds it to the others)
+                float lse_v = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -INFINITY, fac = 1.f;
+                if (direct && p.sinks != nullptr) {
+                    const float tot = log_add_exp(lse_v, p.sinks[h * C::G + g]);
+                    fac = (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
+                    lse_v = tot;
+                }
+                sm_fin[C::G + g] = fac;
+                sm_fin[2 * C::G + g] = lse_v;
             }
             named_barrier_sync(1, C::NCW * 32);
             const size_t row0 = (size_t)j * p.H_q + (size_t)h * C::G;  // row of head g = row0 + g
@@ -529,7 +555,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
 #pragma unroll
                 for (int w = 0; w < C::NCW; ++w) u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
                 const float Ls = sm_fin[g];
-                const float o = (Ls > 0.f) ? (u / Ls) * vscale : 0.f;
+                const float o = (Ls > 0.f) ? (u / Ls) * vscale * sm_fin[C::G + g] : 0.f;
                 if (direct)
                     reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * rows + row0 + g) * D + d] =
                         __float2bfloat16_rn(o);
@@ -538,8 +564,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
             }
             if (ctid < C::G) {
                 const int g = ctid;
-                const float Ls = sm_fin[g];
-                const float v = (Ls > 0.f) ? (sm_fin[C::G + g] + log2f(Ls)) * kLn2 : -INFINITY;
+                const float v = sm_fin[2 * C::G + g];
                 if (direct)
                     p.lse[(size_t)sb * rows + row0 + g] = v;
                 else if (split_ok)
@@ -550,11 +575,11 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
     }
 }
 
-template <int D, bool FP8, int NQ>
+template <int D, bool FP8, int NQ, bool WIN>
 static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
                               bool pdl) {
     using C = GqaCfg<D, FP8, NQ>;
-    auto kern = gqa_decode_kernel<D, FP8, NQ>;
+    auto kern = gqa_decode_kernel<D, FP8, NQ, WIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -572,16 +597,21 @@ static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, con
 
 cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p,
                        cudaStream_t stream, bool pdl) {
-    if (p.s_q == 1) {
-        if (!fp8 && D == 64) return launch_one<64, false, 1>(tkv, tv, p, stream, pdl);
-        if (!fp8 && D == 128) return launch_one<128, false, 1>(tkv, tv, p, stream, pdl);
-        if (fp8 && D == 128) return launch_one<128, true, 1>(tkv, tv, p, stream, pdl);
+    // one token without a window: the lean build; every other shape carries the window logic
+    if (p.s_q == 1 && p.window == 0) {
+        if (!fp8 && D == 64) return launch_one<64, false, 1, false>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 1, false>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 1, false>(tkv, tv, p, stream, pdl);
+    } else if (p.s_q == 1) {
+        if (!fp8 && D == 64) return launch_one<64, false, 1, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 1, true>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 1, true>(tkv, tv, p, stream, pdl);
     } else if (p.s_q == 2) {
-        if (!fp8 && D == 64) return launch_one<64, false, 2>(tkv, tv, p, stream, pdl);
-        if (!fp8 && D == 128) return launch_one<128, false, 2>(tkv, tv, p, stream, pdl);
-        if (fp8 && D == 128) return launch_one<128, true, 2>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 64) return launch_one<64, false, 2, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 2, true>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 2, true>(tkv, tv, p, stream, pdl);
     } else if (p.s_q <= kMaxSqD64 && !fp8 && D == 64) {
-        return launch_one<64, false, kMaxSqD64>(tkv, tv, p, stream, pdl);
+        return launch_one<64, false, kMaxSqD64, true>(tkv, tv, p, stream, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -165,8 +165,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     const int4 rec0 = p.meta.parts[2 * part];
     const int4 rec1 = p.meta.parts[2 * part + 1];
     const int32_t *hd = p.meta.header;
-    const bool meta_ok = hd[kHMagic] == kMetaMagic && hd[kHB] == p.B && hd[kHHkv] == 1 && hd[kHG] == p.H_q &&
-                         hd[kHSplits] == p.splits && hd[kHNumParts] == p.num_parts && (int)gridDim.x == p.num_parts;
+    const bool meta_ok = meta_header_ok(load_meta_header(hd), p.B, 1, p.H_q, p.splits, p.num_parts, 1, 0) &
+                         ((int)gridDim.x == p.num_parts);
     const int max_len = p.max_pages * p.page_size;
 
     if (!meta_ok) {

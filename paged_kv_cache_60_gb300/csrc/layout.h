@@ -31,7 +31,8 @@ enum MetaHeader : int {
     kHKvDtype = 13,
     kHNumSms = 14,
     kHSq = 15,
-    kHeaderWords = 16,
+    kHWindow = 16,
+    kHeaderWords = 32,
 };
 
 // One part record (32 bytes): the part's first request b0, that request's
@@ -69,7 +70,16 @@ struct SchedParams {
     int32_t *split_offset;
     int32_t *num_splits;
     int32_t B, H_kv, G, splits, num_parts, cpc, max_len, kv_dtype, num_sms, s_q;
+    int32_t window;          // sliding window in tokens, 0: none
 };
+
+// First token that any of a request's s_q query tokens sees, with a sliding
+// window of `window` tokens (0: none): the chunks before the one holding it
+// are never read (XQA page, section "分页 KV:页号怎么变成 TMA 坐标").
+__host__ __device__ inline int window_start(int L, int s_q, int window) {
+    const int st = L - s_q + 1 - window;
+    return (window > 0 && st > 0) ? st : 0;
+}
 
 struct GqaParams {
     const void *q;                 // bf16 [B][s_q][H_q][D]
@@ -82,6 +92,8 @@ struct GqaParams {
     float *lse;                    // [B][s_q][H_q]
     int32_t B, H_kv, G, H_q, max_pages, num_pages, page_size, box_tokens, boxes_per_chunk;
     int32_t s_q;                   // query tokens per request (draft j sees L - s_q + 1 + j tokens)
+    int32_t window;                // sliding window in tokens (0: none)
+    const float *sinks;            // [H_q] attention-sink logits (natural-log units) or null
     int32_t log2_box_tokens;       // box_tokens is 8, 16, 32 or 64
     int32_t kv_swap;               // 1: the V pool lies below the K pool (its rows come first in a box)
     int32_t kv_combined;           // 1: one 5-D map covers both pools; 0: one 4-D map per pool
@@ -114,6 +126,8 @@ struct CombineParams {
     void *out;       // bf16 [B][rows][D_v]
     float *lse;      // [B][rows]
     int32_t B, rows, D_v, H_kv, G, splits, num_parts, s_q;   // rows = s_q * H_q per request
+    int32_t window;
+    const float *sinks;  // [H_q] or null: joins each row's denominator after the merge
 };
 
 struct AppendParams {

@@ -9,6 +9,8 @@
 //     split s = [s*per, min((s+1)*per, n_b)).
 //   auto mode (splits = 0): the concatenated chunk sequence of all requests is
 //     cut into num_parts intervals of per = ceil(total / num_parts) chunks.
+// With a sliding window, a request's chunks start at the one holding the
+// first token its first query token sees.
 // One CTA of 1024 threads; block-wide scans over tiles of 1024 requests.
 #include <cuda_runtime.h>
 
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
                 atomicOr(&s_err, DA_DEV_SEQ_TOO_LONG);
                 L = p.max_len;
             }
-            n = (L + kChunk - 1) / kChunk;
+            n = (L + kChunk - 1) / kChunk - window_start(L, p.s_q, p.window) / kChunk;
         }
         int tile_total;
         const int incl = block_incl_scan(n, warp_sums, tile_total);
@@ -179,6 +181,8 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
         h[kHKvDtype] = p.kv_dtype;
         h[kHNumSms] = p.num_sms;
         h[kHSq] = p.s_q;
+        h[kHWindow] = p.window;
+        for (int k = kHWindow + 1; k < kHeaderWords; ++k) h[k] = 0;
     }
 }
 

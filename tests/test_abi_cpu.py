@@ -50,7 +50,7 @@ def test_sched_meta_bytes_and_parts_host_only(lib):
     d = _desc()
     n = da.sched_meta_bytes(d)
     offs = da.meta_offsets(d)
-    assert offs[7] == n and offs[0] == 0 and offs[1] == 64
+    assert offs[7] == n and offs[0] == 0 and offs[1] == 128
     assert all(o % 16 == 0 for o in offs)
     assert offs[5] % 256 == 0 and offs[6] % 256 == 0
     assert da.num_parts(d) == auto_num_parts(152, 2, 1) == 76
