@@ -8,7 +8,8 @@ benchmark's CPU-baseline leg may import this package; the library under
   head range, token range), plus the split merge; built with gcc + OpenMP.
   ``attend_multi`` applies it per query token of the general decode step:
   several query tokens per request (each draft sees the history and the
-  drafts before it), a sliding window, attention sinks.
+  drafts before it), a sliding window, attention sinks; ``attend_sparse``
+  over a list of token positions per request (top-k sparse decode).
 * ``sched_ref.py``  -- the integer split-KV scheduling metadata.
 * ``append_ref.py`` -- appending one new token per request into its page slot,
   with the e4m3 encoder (per-head scales, or the 656-byte latent token).
@@ -64,6 +65,9 @@ def _load():
             lib.ref_attend_units.restype = ctypes.c_int
             lib.ref_attend_units.argtypes = [ctypes.POINTER(RefDesc), P, P, P, P, P, P, P,
                                              ctypes.c_int, P, P, ctypes.c_int64, P, ctypes.c_int64]
+            lib.ref_attend_lists.restype = ctypes.c_int
+            lib.ref_attend_lists.argtypes = [ctypes.POINTER(RefDesc), P, P, P, P, P, P, ctypes.c_int, P, P,
+                                             P, ctypes.c_int64, P, ctypes.c_int64]
             lib.ref_combine.restype = None
             lib.ref_combine.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P]
             lib.ref_e4m3_value.restype = ctypes.c_double
@@ -186,6 +190,52 @@ def attend_multi(w, heads=None):
         fac = torch.where(torch.isneginf(lse), torch.zeros_like(lse), torch.exp(lse - tot))
         out = torch.where(done.unsqueeze(-1), out * fac.unsqueeze(-1), out)
         lse = torch.where(done, tot, lse)
+    return out, lse
+
+
+def attend_sparse(w, indices=None, heads=None):
+    """Sparse (top-k) decode, the FlashMLA page's decode call with `indices`:
+    request b attends over the token positions indices[b, :] (int32 [B, topk];
+    defaults to w.indices). Entries outside [0, L_b) -- the -1 padding of a
+    short request, or a stale position -- are skipped; a position listed twice
+    is two terms. Returns out [B, H_q, D_v] and lse [B, H_q] (float64; NaN
+    where not computed; lse -inf and out 0 for a request with no valid entry)."""
+    lib = _load()
+    s = w.spec
+    if indices is None:
+        indices = w.indices
+    idx = indices.to(torch.int32).cpu()
+    if heads is None:
+        heads = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
+    toks, units = [], []
+    for (b, h) in heads:
+        L = w.lengths[b]
+        lst = [int(t) for t in idx[b].tolist() if 0 <= int(t) < L]
+        units.append((b, h, 0, s.G, len(toks), len(lst)))
+        toks.extend(lst)
+    q64 = w.q.to(torch.float64).contiguous()
+    d = RefDesc(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, P=s.page_size,
+                max_pages=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=_kv_tag(w),
+                pad=0, softmax_scale=w.softmax_scale)
+    n = len(units)
+    u_arr = torch.tensor(units, dtype=torch.int32).reshape(n, 6).contiguous()
+    t_arr = torch.tensor(toks if toks else [0], dtype=torch.int32)
+    o = torch.zeros(n, s.G, s.D_v, dtype=torch.float64)
+    l = torch.zeros(n, s.G, dtype=torch.float64)
+    kp = w.k_pool.contiguous()
+    vp = w.v_pool.contiguous() if w.v_pool is not None else None
+    ks = w.k_scale.contiguous() if w.k_scale is not None else None
+    vs = w.v_scale.contiguous() if w.v_scale is not None else None
+    bt = w.block_table.contiguous()
+    bad = lib.ref_attend_lists(ctypes.byref(d), _ptr(q64), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(bt),
+                               n, _ptr(u_arr), _ptr(t_arr), _ptr(o), s.G * s.D_v, _ptr(l), s.G)
+    if bad:
+        raise ValueError(f"oracle: {bad} unit(s) read a page id outside the pool")
+    out = torch.full((s.B, s.H_q, s.D_v), float("nan"), dtype=torch.float64)
+    lse = torch.full((s.B, s.H_q), float("nan"), dtype=torch.float64)
+    for i, (b, h) in enumerate(heads):
+        out[b, h * s.G:(h + 1) * s.G] = o[i]
+        lse[b, h * s.G:(h + 1) * s.G] = l[i]
     return out, lse
 
 

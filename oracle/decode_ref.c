@@ -140,16 +140,18 @@ static int gather_token(const ref_desc *d, const void *k_pool, const void *v_poo
 }
 
 /*
- * Attention of heads g in [g0, g1) of (b, h) over tokens [t0, t1).
+ * Attention of heads g in [g0, g1) of (b, h) over n tokens: token i is
+ * toks[i] when toks is not NULL (a list, for sparse decode), else t0 + i (the
+ * range [t0, t0 + n)).
  * q64: float64 queries [B][H_kv*G][D_qk]. Writes out[(g1-g0)][D_v], lse[g1-g0].
  * Returns 0, or -1 on a bad page id.
  */
-static int attend_range(const ref_desc *d, const double *q64, const void *k_pool,
-                        const void *v_pool, const float *k_scale, const float *v_scale,
-                        const int32_t *block_table, int b, int h, int g0, int g1,
-                        int t0, int t1, double *out, double *lse)
+static int attend_tokens(const ref_desc *d, const double *q64, const void *k_pool,
+                         const void *v_pool, const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, int b, int h, int g0, int g1,
+                         const int32_t *toks, int t0, int n, double *out, double *lse)
 {
-    int ng = g1 - g0, n = t1 - t0;
+    int ng = g1 - g0;
     int Dq = d->D_qk, Dv = d->D_v, Hq = d->H_kv * d->G;
     memset(out, 0, sizeof(double) * (size_t)ng * Dv);
     if (n <= 0) {
@@ -162,7 +164,7 @@ static int attend_range(const ref_desc *d, const double *q64, const void *k_pool
     int rc = 0;
     /* scores */
     for (int i = 0; i < n && rc == 0; i++) {
-        if (gather_token(d, k_pool, v_pool, k_scale, v_scale, block_table, b, h, t0 + i, k, v)) {
+        if (gather_token(d, k_pool, v_pool, k_scale, v_scale, block_table, b, h, toks ? toks[i] : t0 + i, k, v)) {
             rc = -1;
             break;
         }
@@ -183,7 +185,7 @@ static int attend_range(const ref_desc *d, const double *q64, const void *k_pool
         }
         /* weighted sum of V */
         for (int i = 0; i < n; i++) {
-            gather_token(d, k_pool, v_pool, k_scale, v_scale, block_table, b, h, t0 + i, k, v);
+            gather_token(d, k_pool, v_pool, k_scale, v_scale, block_table, b, h, toks ? toks[i] : t0 + i, k, v);
             for (int g = 0; g < ng; g++) {
                 double w = exp(s[(size_t)g * n + i] - lse[g]);
                 double *o = out + (size_t)g * Dv;
@@ -214,9 +216,34 @@ int ref_attend_units(const ref_desc *d, const double *q64, const void *k_pool,
     for (int u = 0; u < n_units; u++) {
         const int32_t *r = units + 6 * u;
         int t1 = r[5] < 0 ? seqlens[r[0]] : r[5];
-        if (attend_range(d, q64, k_pool, v_pool, k_scale, v_scale, block_table, r[0], r[1],
-                         r[2], r[3], r[4], t1, out + (int64_t)u * out_stride,
-                         lse + (int64_t)u * lse_stride))
+        if (attend_tokens(d, q64, k_pool, v_pool, k_scale, v_scale, block_table, r[0], r[1],
+                          r[2], r[3], NULL, r[4], t1 - r[4], out + (int64_t)u * out_stride,
+                          lse + (int64_t)u * lse_stride))
+            bad++;
+    }
+    return bad;
+}
+
+/*
+ * Sparse decode (FlashMLA page, the decode call with top-k `indices`): unit u
+ * {b, h, g0, g1, off, n} attends over the n token positions tokens[off ..
+ * off + n) of request b (the caller keeps only positions inside [0, L_b); a
+ * position listed twice is two terms of the sum). Outputs as in
+ * ref_attend_units. Returns the number of units that hit a bad page id.
+ */
+int ref_attend_lists(const ref_desc *d, const double *q64, const void *k_pool,
+                     const void *v_pool, const float *k_scale, const float *v_scale,
+                     const int32_t *block_table, int n_units, const int32_t *units,
+                     const int32_t *tokens, double *out, int64_t out_stride, double *lse,
+                     int64_t lse_stride)
+{
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int u = 0; u < n_units; u++) {
+        const int32_t *r = units + 6 * u;
+        if (attend_tokens(d, q64, k_pool, v_pool, k_scale, v_scale, block_table, r[0], r[1],
+                          r[2], r[3], tokens + r[4], 0, r[5], out + (int64_t)u * out_stride,
+                          lse + (int64_t)u * lse_stride))
             bad++;
     }
     return bad;

@@ -38,6 +38,7 @@ class WorkloadSpec:
     s_q: int = 1                        # query tokens per request (draft tokens of a linear chain)
     window: int = 0                     # sliding window in tokens (0: none)
     sinks: bool = False                 # one attention-sink logit per query head
+    topk: int = 0                       # sparse decode: token positions listed per request (0: dense)
     description: str = field(default="", compare=False)
 
     @property

@@ -60,6 +60,7 @@ class Workload:
     block_table: torch.Tensor       # int32 [B, max_pages_per_seq]
     cache_seqlens: torch.Tensor     # int32 [B]
     sinks: Optional[torch.Tensor] = None  # fp32 [H_q] attention-sink logits, or None
+    indices: Optional[torch.Tensor] = None  # int32 [B, topk] token positions (sparse decode), or None
 
     @property
     def softmax_scale(self) -> float:
@@ -69,7 +70,9 @@ class Workload:
     def kv_bytes(self) -> int:
         """Bytes of K and V that a decode pass must read once per KV head."""
         s = self.spec
-        if s.window > 0:   # tokens before the first query token's window are not read
+        if s.topk > 0:     # sparse decode reads the listed tokens (each valid entry once)
+            tok = int(sum(min(L, s.topk) for L in self.lengths))
+        elif s.window > 0:   # tokens before the first query token's window are not read
             tok = int(sum(L - max(0, L - s.s_q + 1 - s.window) for L in self.lengths if L > 0))
         else:
             tok = int(sum(self.lengths))
@@ -226,9 +229,20 @@ def make_workload(spec: WorkloadSpec, lengths: Optional[List[int]] = None,
         # per query head, around ln 64: a sink worth tens of tokens of weight
         gs = torch.Generator().manual_seed(spec.seed + 17)
         sinks = (torch.randn(H_q, generator=gs) * 2.0 + math.log(64.0)).float()
+    indices = None
+    if spec.topk > 0:
+        # top-k positions per request: topk distinct positions in random order,
+        # or, for a request shorter than topk, all of its positions then -1
+        gi = torch.Generator().manual_seed(spec.seed + 29)
+        indices = torch.full((B, spec.topk), -1, dtype=torch.int32)
+        for b, L in enumerate(lengths):
+            if L > 0:
+                pick = torch.randperm(L, generator=gi)[:spec.topk].to(torch.int32)
+                indices[b, :pick.numel()] = pick
     return Workload(spec=spec, lengths=lengths, num_pages=num_pages, max_pages_per_seq=maxp,
                     q=q, k_pool=k_pool, v_pool=v_pool, k_scale=k_scale, v_scale=v_scale,
-                    block_table=bt, cache_seqlens=torch.tensor(lengths, dtype=torch.int32), sinks=sinks)
+                    block_table=bt, cache_seqlens=torch.tensor(lengths, dtype=torch.int32), sinks=sinks,
+                    indices=indices)
 
 
 def place_logical(w: Workload, b: int, t: int, k_row=None, v_row=None):
@@ -260,7 +274,8 @@ def repermute_pages(w: Workload, seed: int) -> Workload:
                     max_pages_per_seq=w.max_pages_per_seq, q=w.q.clone(),
                     k_pool=move(w.k_pool), v_pool=move(w.v_pool),
                     k_scale=w.k_scale, v_scale=w.v_scale,
-                    block_table=bt.to(torch.int32), cache_seqlens=w.cache_seqlens.clone(), sinks=w.sinks)
+                    block_table=bt.to(torch.int32), cache_seqlens=w.cache_seqlens.clone(), sinks=w.sinks,
+                    indices=w.indices)
 
 
 def make_append_batch(w: Workload, seed: int):
