@@ -169,7 +169,8 @@ def make_desc(da, w):
     s = w.spec
     return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,
                         max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=s.kv_dtype,
-                        splits=s.splits, softmax_scale=s.softmax_scale, s_q=s.s_q, window=s.window)
+                        splits=s.splits, softmax_scale=s.softmax_scale, s_q=s.s_q, window=s.window,
+                        topk=s.topk)
 
 
 class DevCopy:
@@ -183,6 +184,7 @@ class DevCopy:
         self.block_table = w.block_table.to(dev)
         self.cache_seqlens = w.cache_seqlens.to(dev)
         self.sinks = w.sinks.to(dev) if w.sinks is not None else None
+        self.indices = w.indices.to(dev) if w.indices is not None else None
         s = w.spec
         self.meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device=dev)
         self.out = torch.empty(s.B, s.s_q * s.H_q, s.D_v, dtype=torch.bfloat16, device=dev)
@@ -203,7 +205,8 @@ class DevCopy:
 
     def fwd(self, da, desc, stream, **kw):
         da.fwd(desc, self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale, self.block_table,
-               self.cache_seqlens, self.meta, self.out, self.lse, stream=stream, sinks=self.sinks, **kw)
+               self.cache_seqlens, self.meta, self.out, self.lse, stream=stream, sinks=self.sinks,
+               indices=self.indices, **kw)
 
     def step(self, da, desc, stream, **kw):
         self.sched(da, desc, stream)
@@ -215,9 +218,14 @@ def oracle_time_per_call(w, budget_s):
     units, scaled to one whole call. Returns (us_per_call, cores, sample text)."""
     import oracle
     s = w.spec
-    attend = oracle.attend_multi if s.s_q > 1 else oracle.attend
+    if s.topk > 0:
+        attend = oracle.attend_sparse
+    elif s.s_q > 1 or s.window > 0 or s.sinks:
+        attend = oracle.attend_multi
+    else:
+        attend = oracle.attend
     units_all = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
-    cost = {u: w.lengths[u[0]] for u in units_all}
+    cost = {u: (min(w.lengths[u[0]], s.topk) if s.topk > 0 else w.lengths[u[0]]) for u in units_all}
     total_cost = sum(cost.values())
     # cheap probe on the shortest unit to size the sample
     probe = min(units_all, key=lambda u: cost[u])
@@ -412,7 +420,8 @@ def run_ours(args, rank, world, local):
     hbm_achieved = kv_bytes / (main_ms * 1e-3) / 1e9
     if key == "mla":
         # tensor-bound: 2 (D_qk + D_v) flops per (token, query head); 424 flop per KV byte
-        flops = 2.0 * (spec.D_qk + spec.D_v) * spec.H_q * sum(w.lengths)
+        ntok = sum(min(L, spec.topk) for L in w.lengths) if spec.topk > 0 else sum(w.lengths)
+        flops = 2.0 * (spec.D_qk + spec.D_v) * spec.H_q * ntok
         achieved = flops / (main_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": round(achieved / tc_peak, 4), "traffic": traffic,
@@ -428,7 +437,8 @@ def run_ours(args, rank, world, local):
     e2e = None
     with torch.cuda.stream(stream):
         host = {k: getattr(devs[0], k).cpu().pin_memory() for k in
-                ("q", "k_pool", "v_pool", "k_scale", "v_scale", "block_table", "cache_seqlens", "sinks")
+                ("q", "k_pool", "v_pool", "k_scale", "v_scale", "block_table", "cache_seqlens", "sinks",
+                 "indices")
                 if getattr(devs[0], k) is not None}
         h_out = torch.empty_like(devs[0].out, device="cpu").pin_memory()
         h_lse = torch.empty_like(devs[0].lse, device="cpu").pin_memory()
@@ -473,7 +483,7 @@ def run_ours(args, rank, world, local):
                 spec.kv_dtype, "fp8-e4m3 656-byte kv dequantised to bf16 / bf16 q,out"),
             "data": "synthetic",
             "config": {"workload": args.workload, "desc": spec.description, "B": spec.B, "s_q": spec.s_q,
-                       "window": spec.window, "sinks": spec.sinks,
+                       "window": spec.window, "sinks": spec.sinks, "topk": spec.topk,
                        "H_q": spec.H_q,
                        "H_kv": spec.H_kv, "D_qk": spec.D_qk, "D_v": spec.D_v, "page_size": spec.page_size,
                        "splits": spec.splits, "kv_bytes_per_call": kv_bytes,

@@ -78,6 +78,7 @@ typedef struct {
     float softmax_scale;       /* sigma; 0: 1/sqrt(D_qk) */
     int32_t s_q;               /* query tokens per request (0 means 1); see decode_attn_fwd */
     int32_t window;            /* sliding window W in tokens (0: none); see decode_attn_fwd */
+    int32_t topk;              /* sparse decode: positions listed per request (0: dense); see decode_attn_fwd */
 } da_desc;
 
 /* Return codes. */
@@ -113,7 +114,7 @@ int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
  * header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part,
  * total size. Header (32 int32): magic, B, H_kv, G, splits, num_parts, cpc,
  * chunk (64), total_chunks, total_splits, per, error word, error detail,
- * kv_dtype, num_sms, s_q, window, then zeros. parts: num_parts records of 8 int32
+ * kv_dtype, num_sms, s_q, window, topk, then zeros. parts: num_parts records of 8 int32
  * {b0, s0, c0, c1, co0, L0, so0, ns0}: first request, its split index there,
  * global chunk interval [c0, c1), then chunk_offset[b0], min(L_b0,
  * max_pages_per_seq*page_size), split_offset[b0], num_splits[b0] (all 0 when
@@ -137,7 +138,8 @@ int decode_attn_num_parts(const da_desc *desc, int32_t *num_parts);
  * one holding token max(0, L_b - s_q + 1 - W), the first its first query token
  * sees: the pages before it are never read (XQA page, section
  * "分页 KV:页号怎么变成 TMA 坐标"), and their block_table entries may hold
- * anything.
+ * anything. Sparse decode (desc->topk = k > 0) gives every request k slots,
+ * ceil(k / 64) chunks, whatever its length.
  * cache_seqlens: device int32 [B]. sched_meta: device, caller-owned, at least
  * decode_attn_sched_meta_bytes. Launches one small kernel on `stream`; the
  * result may be reused by any number of decode_attn_fwd calls while
@@ -169,6 +171,15 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
  * a row that sees no token gets out = 0 and lse = sink. Both are for the
  * bf16 and e4m3 formats (DA_ERR_UNSUPPORTED with the 656-byte format).
  *
+ * Sparse top-k decode (desc->topk = k > 0, da_launch_opts.indices; the
+ * FlashMLA page's decode call with `indices`, ledger rows "FP8 稀疏解码"): for
+ * the 656-byte format only. indices is device int32 [B][k]; request b attends
+ * over the token positions indices[b][0..k) instead of [0, L_b): each is a
+ * position in the request, mapped through block_table like a dense token;
+ * entries outside [0, L_b) (-1 padding, stale positions) are skipped, and a
+ * position listed twice counts twice. A request with no valid entry gets
+ * out = 0, lse = -inf. Pages that no listed position touches are never read.
+ *
  *   q:            bf16 [B][H_kv*G][D_qk], query head h*G+g belongs to KV head h
  *   k_pool/v_pool: see da_kv_dtype
  *   k_scale/v_scale: fp32 [H_kv] for DA_KV_FP8_PER_TENSOR, else ignored
@@ -190,6 +201,7 @@ typedef struct {
     cudaEvent_t main_begin;   /* if not NULL: recorded on `stream` just before the split-KV kernel */
     cudaEvent_t main_end;     /* if not NULL: recorded just after it (before the combine kernel) */
     const float *sinks;       /* if not NULL: device fp32 [H_kv*G] attention-sink logits (see decode_attn_fwd) */
+    const int32_t *indices;   /* sparse decode (desc->topk > 0): device int32 [B][topk] token positions */
 } da_launch_opts;
 
 /* decode_attn_fwd with launch options and optional inputs (opts may be NULL). */

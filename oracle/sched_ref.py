@@ -9,7 +9,9 @@ unless a sliding window of W tokens is set: then the first query token (of s_q
 per request) sees tokens from start_b = max(0, L_b - s_q + 1 - W) on, and the
 chunks before the one holding start_b are never read, f_b = floor(start_b / C)
 (XQA page, section "分页 KV:页号怎么变成 TMA 坐标": with a sliding window the
-leading pages are skipped).
+leading pages are skipped). Sparse top-k decode reads topk listed positions per
+request, so n_b = ceil(topk / C) whatever L_b (FlashMLA page: the metadata call
+takes topk).
 
 * Fixed mode (splits = S > 0) follows the split range of FlashAttention's
   block.h (FlashAttention tiling page, section 5.3 "Split 在 block.h 中的实现"):
@@ -65,9 +67,12 @@ class SchedRef:
 
 
 def sched_ref(seqlens: List[int], H_kv: int, splits: int, num_sms: int, cpc: int = 1, window: int = 0,
-              s_q: int = 1) -> SchedRef:
+              s_q: int = 1, topk: int = 0) -> SchedRef:
     B = len(seqlens)
-    n = [ceil_div(max(0, L), CHUNK) - first_chunk(L, window, s_q) for L in seqlens]
+    if topk > 0:   # sparse decode: every request has topk listed positions to read
+        n = [ceil_div(topk, CHUNK)] * B
+    else:
+        n = [ceil_div(max(0, L), CHUNK) - first_chunk(L, window, s_q) for L in seqlens]
     chunk_offset = [0]
     for x in n:
         chunk_offset.append(chunk_offset[-1] + x)

@@ -37,18 +37,19 @@ class Desc(ctypes.Structure):
                 ("D_qk", ctypes.c_int32), ("D_v", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float), ("s_q", ctypes.c_int32), ("window", ctypes.c_int32)]
+                ("softmax_scale", ctypes.c_float), ("s_q", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("topk", ctypes.c_int32)]
 
     @classmethod
     def make(cls, B, H_kv, G, D_qk, D_v, page_size, max_pages_per_seq, num_pages, kv_dtype=KV_BF16,
-             splits=0, num_sms=0, softmax_scale=0.0, s_q=1, window=0):
+             splits=0, num_sms=0, softmax_scale=0.0, s_q=1, window=0, topk=0):
         return cls(B, H_kv, G, D_qk, D_v, page_size, max_pages_per_seq, num_pages, kv_dtype, splits,
-                   num_sms, softmax_scale, s_q, window)
+                   num_sms, softmax_scale, s_q, window, topk)
 
 
 class LaunchOpts(ctypes.Structure):
     _fields_ = [("use_pdl", ctypes.c_int32), ("main_begin", ctypes.c_void_p), ("main_end", ctypes.c_void_p),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("indices", ctypes.c_void_p)]
 
 
 class DecodeAttnError(RuntimeError):
@@ -131,12 +132,12 @@ def sched_meta(desc: Desc, cache_seqlens, meta, stream=None, lib=None):
 
 
 def fwd(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seqlens, meta, out, lse,
-        stream=None, use_pdl=True, main_begin=None, main_end=None, sinks=None, lib=None):
+        stream=None, use_pdl=True, main_begin=None, main_end=None, sinks=None, indices=None, lib=None):
     lib = lib or load_library()
     args = (ctypes.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
             _ptr(block_table), _ptr(cache_seqlens), _ptr(meta), meta.numel() * meta.element_size(),
             _ptr(out), _ptr(lse))
-    if use_pdl and main_begin is None and main_end is None and sinks is None:
+    if use_pdl and main_begin is None and main_end is None and sinks is None and indices is None:
         _check(lib.decode_attn_fwd(*args, _stream(stream)))
     else:
         def ev(e):
@@ -146,7 +147,8 @@ def fwd(desc: Desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seql
                 e.record()
             return ctypes.c_void_p(e.cuda_event)
         opts = LaunchOpts(1 if use_pdl else 0, ev(main_begin), ev(main_end),
-                          None if sinks is None else ctypes.c_void_p(sinks.data_ptr()))
+                          None if sinks is None else ctypes.c_void_p(sinks.data_ptr()),
+                          None if indices is None else ctypes.c_void_p(indices.data_ptr()))
         _check(lib.decode_attn_fwd_ex(*args, ctypes.byref(opts), _stream(stream)))
 
 

@@ -49,6 +49,7 @@ int check_desc(const da_desc *d) {
     if (!(d->softmax_scale >= 0.f) || std::isinf(d->softmax_scale)) return DA_ERR_DIMS;
     if (d->s_q < 0 || d->s_q > 64) return DA_ERR_DIMS;
     if (d->window < 0) return DA_ERR_DIMS;
+    if (d->topk < 0 || d->topk > (1 << 24)) return DA_ERR_DIMS;
     const int sq = sq_of(d);
     const int P = d->page_size;
     const bool page_ok = (P == 8 || P == 16 || P == 32 || (P % 64) == 0);
@@ -56,11 +57,11 @@ int check_desc(const da_desc *d) {
     switch (d->kv_dtype) {
         case DA_KV_BF16:
             if (d->G != 8 || d->D_qk != d->D_v || (d->D_qk != 64 && d->D_qk != 128)) return DA_ERR_UNSUPPORTED;
-            if (sq > (d->D_qk == 64 ? kMaxSqD64 : kMaxSqD128)) return DA_ERR_UNSUPPORTED;
+            if (sq > (d->D_qk == 64 ? kMaxSqD64 : kMaxSqD128) || d->topk != 0) return DA_ERR_UNSUPPORTED;
             break;
         case DA_KV_FP8_PER_TENSOR:
             if (d->G != 8 || d->D_qk != 128 || d->D_v != 128) return DA_ERR_UNSUPPORTED;
-            if (sq > kMaxSqD128) return DA_ERR_UNSUPPORTED;
+            if (sq > kMaxSqD128 || d->topk != 0) return DA_ERR_UNSUPPORTED;
             break;
         case DA_KV_FP8_MLA656:
             if (d->H_kv != 1 || d->D_qk != 576 || d->D_v != 512 || d->G != 128) return DA_ERR_UNSUPPORTED;
@@ -271,6 +272,7 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens, vo
     p.num_sms = nsm;
     p.s_q = sq_of(desc);
     p.window = desc->window;
+    p.topk = desc->topk;
     if (launch_sched_meta(p, stream, true) != cudaSuccess) return DA_ERR_CUDA;
     return DA_OK;
 }
@@ -298,6 +300,9 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
     const float *sinks = opts ? opts->sinks : nullptr;
     if (sinks && mla) return DA_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(sinks) & 3u) return DA_ERR_ALIGN;
+    const int32_t *indices = opts ? opts->indices : nullptr;
+    if (desc->topk > 0 && !indices) return DA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(indices) & 3u) return DA_ERR_ALIGN;
     const bool pdl = opts ? opts->use_pdl != 0 : true;
     const float sigma = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->D_qk);
     const MetaView mv = meta_view(sched_meta, L);
@@ -377,6 +382,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitLimitNs;
         p.page_trace = g_page_trace;
         p.page_trace_cap = g_page_trace_cap;
+        p.indices = desc->topk > 0 ? indices : nullptr;
+        p.topk = desc->topk;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     }
@@ -389,6 +396,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
     c.rows = H_q * sq_of(desc);
     c.s_q = sq_of(desc);
     c.window = desc->window;
+    c.topk = desc->topk;
     c.sinks = sinks;
     c.D_v = desc->D_v;
     c.H_kv = desc->H_kv;

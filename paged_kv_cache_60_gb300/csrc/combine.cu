@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     const int32_t *hd = p.meta.header;
     const int ns = p.meta.num_splits[b];
     const int so = p.meta.split_offset[b];
-    if (!meta_header_ok(load_meta_header(hd), p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q, p.window))
+    if (!meta_header_ok(load_meta_header(hd), p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q, p.window,
+                        p.topk))
         return;  // the split-KV kernel has flagged the mismatch
     if (hq >= p.rows) return;
     if (ns == 1) return;  // written directly by the split-KV kernel

@@ -28,7 +28,7 @@ __device__ __forceinline__ float log_add_exp(float a, float b) {
 }
 
 // The sched_meta header words the kernels check (magic, B, H_kv, G, splits,
-// num_parts, s_q, window), read with independent 16-byte loads so that their
+// num_parts, s_q, window, topk), read with independent 16-byte loads so that their
 // latencies overlap.
 struct MetaHdr {
     int4 w0, w4, w12, w16;  // words 0-3, 4-7, 12-15, 16-19
@@ -37,14 +37,14 @@ __device__ __forceinline__ MetaHdr load_meta_header(const int32_t *hd) {
     const int4 *v = reinterpret_cast<const int4 *>(hd);
     return MetaHdr{v[0], v[1], v[3], v[4]};
 }
-// magic, B, H_kv, G, splits, num_parts, s_q, window all as expected
+// magic, B, H_kv, G, splits, num_parts, s_q, window, topk all as expected
 __device__ __forceinline__ bool meta_header_ok(const MetaHdr &h, int B, int H_kv, int G, int splits, int num_parts,
-                                               int s_q, int window) {
+                                               int s_q, int window, int topk) {
     static_assert(kHMagic == 0 && kHB == 1 && kHHkv == 2 && kHG == 3 && kHSplits == 4 && kHNumParts == 5 &&
-                      kHSq == 15 && kHWindow == 16,
+                      kHSq == 15 && kHWindow == 16 && kHTopk == 17,
                   "header word positions");
     return (h.w0.x == kMetaMagic) & (h.w0.y == B) & (h.w0.z == H_kv) & (h.w0.w == G) & (h.w4.x == splits) &
-           (h.w4.y == num_parts) & (h.w12.w == s_q) & (h.w16.x == window);
+           (h.w4.y == num_parts) & (h.w12.w == s_q) & (h.w16.x == window) & (h.w16.y == topk);
 }
 
 // ------------------------------------------------------------------ timing

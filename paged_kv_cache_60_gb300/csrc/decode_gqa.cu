@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
     {
         const int32_t *hd = p.meta.header;
         const bool ok = meta_header_ok(load_meta_header(hd), p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q,
-                                       p.window) &
+                                       p.window, 0) &
                         ((int)gridDim.x == p.num_parts);
         if (!ok) {
             if (threadIdx.x == 0) atomicOr(&p.meta.header[kHError], DA_DEV_META_MISMATCH);

@@ -117,6 +117,8 @@ __device__ __forceinline__ void dequant16(const uint4 v, float scale, uint4 &lo,
 }
 
 
+// SPARSE: top-k decode (the tokens are the positions p.indices lists; p.topk > 0)
+template <bool SPARSE>
 __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __grid_constant__ MlaParams p) {
     using namespace mla;
     extern __shared__ uint8_t smem_raw[];
@@ -165,7 +167,8 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     const int4 rec0 = p.meta.parts[2 * part];
     const int4 rec1 = p.meta.parts[2 * part + 1];
     const int32_t *hd = p.meta.header;
-    const bool meta_ok = meta_header_ok(load_meta_header(hd), p.B, 1, p.H_q, p.splits, p.num_parts, 1, 0) &
+    const bool meta_ok = meta_header_ok(load_meta_header(hd), p.B, 1, p.H_q, p.splits, p.num_parts, 1, 0,
+                                        p.topk) &
                          ((int)gridDim.x == p.num_parts);
     const int max_len = p.max_pages * p.page_size;
 
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         while (ok && wk.next(sg)) {
             const int n = sg.lc1 - sg.lc0;
             const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
+            const int32_t *idx_row = p.indices + (size_t)sg.b * p.topk;  // sparse decode only
             for (int c = 0; c < n && ok; ++c) {
                 const int cur = ic + c, kb = cur % NK;
                 const int tbase = (sg.lc0 + c) * kChunk;
@@ -291,16 +295,20 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
 #pragma unroll
                 for (int i = 0; i < 5; ++i) {
                     const int u = dt + 256 * i, tok = u / UNITS, g = u % UNITS;
-                    const int t = tbase + tok;
+                    // dense: token tbase + tok; sparse: the position listed in slot tbase + tok
+                    // (slots past topk and positions outside [0, L) are skipped: a zero row)
+                    int t = tbase + tok;
+                    if (SPARSE) t = t < p.topk ? idx_row[t] : -1;
+                    const bool valid = t >= 0 && t < sg.L;
                     ra[i] = make_uint4(0u, 0u, 0u, 0u);
                     rb[i] = ra[i];
                     sc[i] = 0.f;
 #ifdef DA_PAGE_TRACE
                     if (p.page_trace && rank == 0 && g == 0 && cur < p.page_trace_cap)
                         p.page_trace[((size_t)part * p.page_trace_cap + cur) * kChunk + tok] =
-                            t < sg.L ? bt_row[t / p.page_size] * p.page_size + t % p.page_size : -2;
+                            valid ? bt_row[t / p.page_size] * p.page_size + t % p.page_size : -2;
 #endif
-                    if (t < sg.L) {
+                    if (valid) {
                         const int pg = bt_row[t / p.page_size];
                         if (pg < 0 || pg >= p.num_pages) {
                             atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
@@ -411,6 +419,15 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             float m_used = -INFINITY, l = 0.f;
             for (int c = 0; c < n; ++c) {
                 const int cur = ic + c;
+                const int cbase = (sg.lc0 + c) * kChunk;
+                // sparse decode: this chunk's listed positions (slots lane, lane + 32),
+                // loaded before the waits so that their latency overlaps them
+                int t0 = -1, t1 = -1;
+                if (SPARSE) {
+                    const int32_t *ir = p.indices + (size_t)sg.b * p.topk + cbase;
+                    if (cbase + lane < p.topk) t0 = ir[lane];
+                    if (cbase + lane + 32 < p.topk) t1 = ir[lane + 32];
+                }
                 bool w_ok = mbar_wait_warp(sfull, cur & 1, abort_flag, p.wait_limit_ns);
                 tc_fence_after();
                 float s[64];
@@ -448,12 +465,25 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer);
                 }
-                const int nvalid = sg.L - (sg.lc0 + c) * kChunk;
                 float mx = -INFINITY;
+                if (SPARSE) {
+                    // sparse: slot e counts when it lies before topk and lists a position in
+                    // [0, L); the warp's ballots give the 64 bits (vm0: slots 0-31, vm1: 32-63)
+                    const uint32_t vm0 = __ballot_sync(0xffffffffu, t0 >= 0 && t0 < sg.L);
+                    const uint32_t vm1 = __ballot_sync(0xffffffffu, t1 >= 0 && t1 < sg.L);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    s[e] = (e < nvalid) ? s[e] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, s[e]);
+                    for (int e = 0; e < 64; ++e) {
+                        const bool v = ((e < 32 ? vm0 >> e : vm1 >> (e - 32)) & 1u) != 0u;
+                        s[e] = v ? s[e] * sl2 : -INFINITY;
+                        mx = fmaxf(mx, s[e]);
+                    }
+                } else {
+                    const int nvalid = sg.L - cbase;  // >= 1: tokens of this chunk in the sequence
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        s[e] = (e < nvalid) ? s[e] * sl2 : -INFINITY;
+                        mx = fmaxf(mx, s[e]);
+                    }
                 }
                 // P's columns and O are free once the previous chunk's PV has completed
                 if (cur > 0) w_ok = w_ok && mbar_wait_warp(pfree, (cur - 1) & 1, abort_flag, p.wait_limit_ns);
@@ -486,11 +516,13 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     }
                 }
                 // P row of this head: 64 tokens as bf16 pairs, the A operand of O += P V
+                // (while no token has counted yet, m_used is -inf: exponents from 0 give P = 0)
+                const float base = (SPARSE && m_used == -INFINITY) ? 0.f : m_used;
                 float ps = 0.f;
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2(s[2 * e] - m_used), p1 = ex2(s[2 * e + 1] - m_used);
+                    const float p0 = ex2(s[2 * e] - base), p1 = ex2(s[2 * e + 1] - base);
                     ps += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
@@ -573,7 +605,7 @@ int mla_max_parts() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (const int c = cached[dev].load(std::memory_order_relaxed)) return c;
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM) !=
+    if (cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -588,13 +620,14 @@ int mla_max_parts() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<false>, &cfg) != cudaSuccess) return 0;
     cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM);
+    auto kern = p.topk > 0 ? mla_decode_kernel<true> : mla_decode_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_parts, 2);
@@ -610,7 +643,7 @@ cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, mla_decode_kernel, p);
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace da

@@ -32,6 +32,7 @@ enum MetaHeader : int {
     kHNumSms = 14,
     kHSq = 15,
     kHWindow = 16,
+    kHTopk = 17,
     kHeaderWords = 32,
 };
 
@@ -71,6 +72,7 @@ struct SchedParams {
     int32_t *num_splits;
     int32_t B, H_kv, G, splits, num_parts, cpc, max_len, kv_dtype, num_sms, s_q;
     int32_t window;          // sliding window in tokens, 0: none
+    int32_t topk;            // sparse decode: listed positions per request (0: dense)
 };
 
 // First token that any of a request's s_q query tokens sees, with a sliding
@@ -119,6 +121,8 @@ struct MlaParams {
     uint64_t wait_limit_ns;
     int32_t *page_trace;           // page-trace test build only (null otherwise): rows read, per token
     int32_t page_trace_cap;        // chunks recorded per part
+    const int32_t *indices;        // sparse decode: [B][topk] token positions, or null
+    int32_t topk;                  // 0: dense (tokens [0, L_b))
 };
 
 struct CombineParams {
@@ -126,7 +130,7 @@ struct CombineParams {
     void *out;       // bf16 [B][rows][D_v]
     float *lse;      // [B][rows]
     int32_t B, rows, D_v, H_kv, G, splits, num_parts, s_q;   // rows = s_q * H_q per request
-    int32_t window;
+    int32_t window, topk;
     const float *sinks;  // [H_q] or null: joins each row's denominator after the merge
 };
 

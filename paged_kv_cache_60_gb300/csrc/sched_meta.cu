@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
                 atomicOr(&s_err, DA_DEV_SEQ_TOO_LONG);
                 L = p.max_len;
             }
-            n = (L + kChunk - 1) / kChunk - window_start(L, p.s_q, p.window) / kChunk;
+            // sparse decode: the request's topk listed positions, whatever its length
+            n = p.topk > 0 ? (p.topk + kChunk - 1) / kChunk
+                           : (L + kChunk - 1) / kChunk - window_start(L, p.s_q, p.window) / kChunk;
         }
         int tile_total;
         const int incl = block_incl_scan(n, warp_sums, tile_total);
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
         h[kHNumSms] = p.num_sms;
         h[kHSq] = p.s_q;
         h[kHWindow] = p.window;
-        for (int k = kHWindow + 1; k < kHeaderWords; ++k) h[k] = 0;
+        h[kHTopk] = p.topk;
+        for (int k = kHTopk + 1; k < kHeaderWords; ++k) h[k] = 0;
     }
 }
 

@@ -49,7 +49,7 @@ def make_desc(w, splits=None, num_sms=0):
     return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,
                         max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages, kv_dtype=s.kv_dtype,
                         splits=s.splits if splits is None else splits, num_sms=num_sms,
-                        softmax_scale=s.softmax_scale, s_q=s.s_q, window=s.window)
+                        softmax_scale=s.softmax_scale, s_q=s.s_q, window=s.window, topk=s.topk)
 
 
 class DeviceWorkload:
@@ -63,6 +63,7 @@ class DeviceWorkload:
         self.block_table = w.block_table.to(dev)
         self.cache_seqlens = w.cache_seqlens.to(dev)
         self.sinks = w.sinks.to(dev) if getattr(w, "sinks", None) is not None else None
+        self.indices = w.indices.to(dev) if getattr(w, "indices", None) is not None else None
 
 
 def run(w, splits=None, num_sms=0, dw=None, meta=None, desc=None, out=None, lse=None, stream=None):
@@ -80,7 +81,7 @@ def run(w, splits=None, num_sms=0, dw=None, meta=None, desc=None, out=None, lse=
     if lse is None:
         lse = torch.full(rows, float("nan"), dtype=torch.float32, device="cuda")
     da.fwd(desc, dw.q, dw.k_pool, dw.v_pool, dw.k_scale, dw.v_scale, dw.block_table, dw.cache_seqlens,
-           meta, out, lse, stream=stream, sinks=dw.sinks)
+           meta, out, lse, stream=stream, sinks=dw.sinks, indices=dw.indices)
     return out, lse, meta, desc
 
 

@@ -137,3 +137,10 @@ def test_window_chunks_are_exactly_the_read_ones(seed):
         start = max(0, L - s_q + 1 - W)
         toks = [t for (t0, t1) in ranges[b] for t in range(t0, t1)]
         assert toks == list(range(start, L)) if L > 0 else toks == []
+
+
+def test_sparse_schedule_counts_topk_slots():
+    ref = sched_ref([0, 5, 10000, 64], H_kv=1, splits=0, num_sms=152, cpc=2, topk=100)
+    assert ref.chunk_offset == [0, 2, 4, 6, 8]
+    ref = sched_ref([0, 5, 10000, 64], H_kv=1, splits=3, num_sms=152, cpc=2, topk=2048)
+    assert ref.chunk_offset == [0, 32, 64, 96, 128] and len(ref.parts) == 12

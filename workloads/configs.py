@@ -91,6 +91,12 @@ CONFIGS = [
         name="window_sinks_gqa_bf16", B=32, H_kv=8, G=8, D_qk=128, D_v=128, page_size=64,
         length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1008, window=2048, sinks=True,
         description="B=32 H_q=64 H_kv=8 D=128 P=64 L~U[1024,8192] sliding window 2048, one sink per head"),
+    # sparse top-k decode on the latent-token format: the pages' "FP8 稀疏解码" row
+    # (topk 2048, batch 128, 128 heads); the context length is not given there
+    WorkloadSpec(
+        name="sparse_mla_topk2048", B=128, H_kv=1, G=128, D_qk=576, D_v=512, page_size=64,
+        kv_dtype=KV_MLA656, lengths=[8192] * 128, splits=0, seed=1009, topk=2048,
+        description="B=128 H_q=128 656-byte FP8 tokens, L=8192, top-k 2048 positions per request"),
 ]
 
 
