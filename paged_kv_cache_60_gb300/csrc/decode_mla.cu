@@ -287,9 +287,28 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             const int n = sg.lc1 - sg.lc0;
             const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
             const int32_t *idx_row = p.indices + (size_t)sg.b * p.topk;  // sparse decode only
+            // sparse decode: the positions listed in this thread's slots, loaded one
+            // chunk ahead so that only the block-table and row loads sit on the chain
+            int tnext[5];
+            if (SPARSE) {
+#pragma unroll
+                for (int i = 0; i < 5; ++i) {
+                    const int slot = sg.lc0 * kChunk + (dt + 256 * i) / UNITS;
+                    tnext[i] = (n > 0 && slot < p.topk) ? idx_row[slot] : -1;
+                }
+            }
             for (int c = 0; c < n && ok; ++c) {
                 const int cur = ic + c, kb = cur % NK;
                 const int tbase = (sg.lc0 + c) * kChunk;
+                int tcur[5];
+                if (SPARSE) {
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) {
+                        tcur[i] = tnext[i];
+                        const int slot = tbase + kChunk + (dt + 256 * i) / UNITS;
+                        tnext[i] = (c + 1 < n && slot < p.topk) ? idx_row[slot] : -1;
+                    }
+                }
                 uint4 ra[5], rb[5];
                 float sc[5];
 #pragma unroll
@@ -298,7 +317,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     // dense: token tbase + tok; sparse: the position listed in slot tbase + tok
                     // (slots past topk and positions outside [0, L) are skipped: a zero row)
                     int t = tbase + tok;
-                    if (SPARSE) t = t < p.topk ? idx_row[t] : -1;
+                    if (SPARSE) t = tcur[i];
                     const bool valid = t >= 0 && t < sg.L;
                     ra[i] = make_uint4(0u, 0u, 0u, 0u);
                     rb[i] = ra[i];
