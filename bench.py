@@ -213,6 +213,59 @@ class DevCopy:
         self.fwd(da, desc, stream, **kw)
 
 
+def append_at_scale(torch, da, spec, stream, hbm_peak, reps=50):
+    """decode_attn_append_kv on a large batch of the workload's KV format
+    (16384 requests, or 65536 latent tokens), one page of 16 slots per
+    request, new rows rotating over enough copies to exceed 2x L2: the append
+    kernel's HBM roofline, which decode batch sizes are too small to show."""
+    P = 16
+    mla = spec.kv_dtype == da.KV_MLA656
+    B = 65536 if mla else 16384
+    H, D = (1, 576) if mla else (spec.H_kv, spec.D_qk)
+    g = torch.Generator(device="cuda").manual_seed(spec.seed + 3)
+    desc = da.Desc.make(B=B, H_kv=H, G=spec.G, D_qk=D, D_v=spec.D_v, page_size=P, max_pages_per_seq=1,
+                        num_pages=B, kv_dtype=spec.kv_dtype)
+    if mla:
+        k_pool, v_pool = torch.zeros(B, P, 1, 656, dtype=torch.uint8, device="cuda"), None
+        row_bytes = 2 * 576 + 656
+    else:
+        dt = torch.uint8 if spec.kv_dtype == da.KV_FP8 else torch.bfloat16
+        k_pool = torch.zeros(B, P, H, D, dtype=dt, device="cuda")
+        v_pool = torch.zeros_like(k_pool)
+        es = 1 if spec.kv_dtype == da.KV_FP8 else 2
+        row_bytes = 2 * H * D * (2 + es)
+    scales = torch.rand(H, generator=g, device="cuda") * 0.05 + 0.01
+    bt = torch.randperm(B, generator=g, device="cuda").to(torch.int32).view(B, 1)
+    pos = torch.randint(0, P, (B,), generator=g, device="cuda", dtype=torch.int32)
+    in_bytes = B * H * D * 2 * (1 if mla else 2)
+    ncopy = max(1, -(-2 * L2_BYTES // in_bytes))
+    rows = [(torch.randn(B, H, D, generator=g, device="cuda").to(torch.bfloat16),
+             None if mla else torch.randn(B, H, D, generator=g, device="cuda").to(torch.bfloat16))
+            for _ in range(ncopy)]
+
+    def call(k):
+        kn, vn = rows[k % ncopy]
+        da.append_kv(desc, kn, vn, pos, bt, k_pool, v_pool, None if mla else scales, None if mla else scales,
+                     stream=stream)
+    with torch.cuda.stream(stream):
+        for k in range(5):
+            call(k)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(reps):
+            call(k)
+        b.record(stream)
+        torch.cuda.synchronize()
+    us = a.elapsed_time(b) / reps * 1000.0
+    nbytes = B * row_bytes + 8 * B
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"requests": B, "us_per_call": round(us, 3), "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+            "frac": round(gbs / hbm_peak, 4), "bound": "hbm",
+            "note": "one page of 16 slots per request, random pages and slots, eager launches, "
+                    "new rows rotating over %d copies" % ncopy}
+
+
 def oracle_time_per_call(w, budget_s):
     """Oracle (float64, host cores) on a bounded sample of (request, KV head)
     units, scaled to one whole call. Returns (us_per_call, cores, sample text)."""
@@ -410,7 +463,9 @@ def run_ours(args, rank, world, local):
     else:
         es = 1 if spec.kv_dtype == da.KV_FP8 else 2
         app_bytes = n_app * 2 * spec.H_kv * spec.D_qk * (2 + es) + 8 * spec.B
-    append = {"us_per_call": round(append_us, 3), "algorithmic_bytes": app_bytes,
+    hbm_peak0, _, _ = load_peaks()
+    app_scale = append_at_scale(torch, da, spec, stream, hbm_peak0)
+    append = {"us_per_call": round(append_us, 3), "algorithmic_bytes": app_bytes, "at_scale": app_scale,
               "gbs": round(app_bytes / (append_us * 1e-6) / 1e9, 1), "with_fwd_us": round(append_fwd_us, 3),
               "call": "decode_attn_append_kv: one new token per request into its page slot "
                       "(bf16 rows in, pool format out), then optionally decode_attn_fwd"}

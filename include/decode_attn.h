@@ -158,8 +158,8 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
  * last s_q tokens are already in the pool (L_b counts them) and draft token
  * j < s_q sees the first L_b - s_q + 1 + j tokens -- the history and the
  * drafts up to itself. A row that sees no token gets out = 0, lse = -inf.
- * Supported: s_q <= 4 for bf16 D = 64, s_q <= 2 for D = 128 (bf16, e4m3);
- * the 656-byte format takes s_q = 1. The rows of q, out and lse below are
+ * Supported: s_q <= 4 for the bf16 and e4m3 formats; the 656-byte format
+ * takes s_q = 1. The rows of q, out and lse below are
  * then [B][s_q][H_kv*G]; the scheduling metadata must be built with the same s_q.
  *
  * Sliding window (desc->window = W > 0; XQA page, section

@@ -32,7 +32,8 @@
 //  * several query tokens per request (linear speculative-decoding
 //    verification, XQA page, section "投机解码:XQA 的第二个工作负载"): the
 //    s_q draft tokens' G heads become NQ n8 tiles on the N side, so every K/V
-//    fragment loaded from shared memory feeds NQ MMAs; draft token j sees the
+//    fragment loaded from shared memory feeds NQ MMAs (three or four tokens:
+//    two warps share each chunk, two tokens each); draft token j sees the
 //    tokens [0, L - s_q + j] (a chain: each draft token sees the ones before it).
 //  * every consumer warp takes whole chunks (round robin) as four independent
 //    16-token tiles, so its MMA chains and shuffle reductions interleave, and
@@ -51,7 +52,7 @@ namespace da {
 
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, bool FP8, int NQ>
+template <int D, bool FP8, int NQ, int WPC>
 struct GqaCfg {
     static constexpr int G = 8;
     static constexpr int ES = FP8 ? 1 : 2;
@@ -59,17 +60,20 @@ struct GqaCfg {
     static constexpr int NX = ROW / 128;     // 128-byte halves of a row
     static constexpr int TILE = kChunk * ROW;
     static constexpr int STAGE = 2 * TILE;   // K and V of one chunk
-    // consumer warps (one chunk each, round robin) and ring stages. NS is a
-    // multiple of NCW so that stage s is always consumed by warp s % NCW: a
-    // warp then waits on the phases of a stage one after the other, and never
-    // on a phase two ahead of the barrier's current one (whose parity would
-    // alias an already completed phase).
+    // consumer warps and ring stages. A chunk goes to a group of WPC warps
+    // (round robin over the NG groups; each warp of the group holds NQ of the
+    // query tokens). NS is a multiple of NG so that stage s is always consumed
+    // by group s % NG: a warp then waits on the phases of a stage one after
+    // the other, and never on a phase two ahead of the barrier's current one
+    // (whose parity would alias an already completed phase).
     // With several query tokens (NQ > 1) a warp holds NQ times the state and
-    // the kernel runs one CTA per SM: 7 consumer warps keep at most two warps
-    // on each SM sub-partition, so a thread may use up to 255 registers.
-    static constexpr int NCW = NQ > 1 ? (D == 128 && !FP8 ? 6 : 7) : (FP8 ? 10 : (D == 64 ? 5 : 6));
+    // the kernel runs one CTA per SM: 6 or 7 consumer warps keep at most two
+    // warps on each SM sub-partition, so a thread may use up to 255 registers.
+    static constexpr int NCW =
+        WPC > 1 ? 6 : (NQ > 1 ? (D == 128 && !FP8 ? 6 : 7) : (FP8 ? 10 : (D == 64 ? 5 : 6)));
+    static constexpr int NG = NCW / WPC;
     static constexpr int NS = NCW == 5 ? 5 : NCW;
-    static_assert(NS % NCW == 0, "stage ownership must be fixed per warp");
+    static_assert(NCW % WPC == 0 && NS % NG == 0, "stage ownership must be fixed per warp group");
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int MT = D / 16;
     static constexpr int KS = D / 16;
@@ -82,19 +86,20 @@ struct GqaCfg {
     static constexpr int OFF_BAR = (OFF_FIN + 4 * G * 4 + 7) / 8 * 8;
     static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
-    static constexpr int MIN_BLOCKS = (D == 64 && !FP8 && NQ == 1) ? 2 : 1;
+    static constexpr int MIN_BLOCKS = (D == 64 && !FP8 && NQ == 1 && WPC == 1) ? 2 : 1;
     static_assert(ROW % 128 == 0, "rows must be whole 128-byte boxes");
     static_assert(!FP8 || NX == 1, "fp8 path expects one 128-byte box per row");
 };
 
-// NQ: query tokens per request the kernel is compiled for (s_q <= NQ; tokens
-// j >= s_q are zero rows that are never written). WIN: built with sliding
-// window support (without it, p.window must be 0).
-template <int D, bool FP8, int NQ, bool WIN>
-__global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ>::MIN_BLOCKS)
+// NQ x WPC: query tokens per request the kernel is compiled for (s_q <=
+// NQ * WPC; warp w of a chunk's group holds tokens [(w % WPC) NQ, (w % WPC + 1)
+// NQ), and tokens j >= s_q are zero rows that are never written). WIN: built
+// with sliding window support (without it, p.window must be 0).
+template <int D, bool FP8, int NQ, int WPC, bool WIN>
+__global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP8, NQ, WPC>::MIN_BLOCKS)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ GqaParams p) {
-    using C = GqaCfg<D, FP8, NQ>;
+    using C = GqaCfg<D, FP8, NQ, WPC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *sm_u = reinterpret_cast<float *>(smem + C::OFF_U);
@@ -112,7 +117,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(&full[i], p.boxes_per_chunk);  // one arrival per producer lane
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], WPC);  // every warp of the chunk's group
         }
         *abort_flag = 0;
 #ifdef DA_PAGE_TRACE
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
 
     // ---------------------------------------------------------------- consumers
     const int r8 = lane >> 2, c4 = lane & 3;
+    const int grp = warp / WPC, jo = (warp % WPC) * NQ;  // this warp's group and first query token
     const int lrow = lane & 7, lmat = lane >> 3;
     const int ctid = threadIdx.x;  // 0 .. NCW*32-1
     const float kscale = FP8 ? p.k_scale[h] : 1.f;
@@ -268,12 +274,12 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
         uint32_t qf[C::KS][NQ][2];
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
-            if (j >= p.s_q) {
+            if (jo + j >= p.s_q) {
 #pragma unroll
                 for (int ks = 0; ks < C::KS; ++ks) qf[ks][j][0] = qf[ks][j][1] = 0u;
                 continue;
             }
-            const size_t qrow = (((size_t)sb * p.s_q + j) * p.H_q + (size_t)h * C::G + r8) * D;
+            const size_t qrow = (((size_t)sb * p.s_q + jo + j) * p.H_q + (size_t)h * C::G + r8) * D;
             if constexpr (!FP8) {
                 const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
                     reinterpret_cast<const __nv_bfloat16 *>(p.q) + qrow);
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
         }
 
         for (int lc = lc0; lc < lc1; ++lc, ++i) {
-            if ((i % C::NCW) != warp) continue;  // one warp per chunk, round robin
+            if ((i % C::NG) != grp) continue;  // one warp group per chunk, round robin
             const int stage = i % C::NS;
 #ifdef DA_PAGE_TRACE
             // test build: a wait on a barrier that nothing completes runs out
@@ -399,9 +405,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
             uint32_t pb[4][NQ][2];
 #pragma unroll
             for (int j = 0; j < NQ; ++j) {
-                const int nv = (NQ == 1) ? nvalid : L_first + j - cbase;
-                // with a window, draft j sees tokens from L_first + j - window on
-                const int lv = (WIN && p.window > 0) ? L_first + j - p.window - cbase : -1;
+                const int nv = (NQ * WPC == 1) ? nvalid : L_first + jo + j - cbase;
+                // with a window, draft jo + j sees tokens from L_first + jo + j - window on
+                const int lv = (WIN && p.window > 0) ? L_first + jo + j - p.window - cbase : -1;
                 float sv[4][4];
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -419,8 +425,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
                 const float mn1 = fmaxf(m1[j], warp_max_xor_4_8_16(mx1));
                 // an earlier draft token may have seen no token yet: keep the
                 // exponent base finite so that 2^(-inf - base) = 0, not NaN
-                const float bs0 = (NQ > 1 && mn0 == -INFINITY) ? 0.f : mn0;
-                const float bs1 = (NQ > 1 && mn1 == -INFINITY) ? 0.f : mn1;
+                const float bs0 = (NQ * WPC > 1 && mn0 == -INFINITY) ? 0.f : mn0;
+                const float bs1 = (NQ * WPC > 1 && mn1 == -INFINITY) ? 0.f : mn1;
                 const float al0 = ex2(m0[j] - bs0), al1 = ex2(m1[j] - bs1);
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
@@ -495,91 +501,100 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ>::THREADS, GqaCfg<D, FP8, NQ
         }
 
         // ---------------------------------------------------------- merge warps
-        // one pass per query token of the request (the scratch holds one)
+        // one pass per query token of the request (the scratch holds one);
+        // token jj = ow * NQ + jl lives in tile jl of the warps with warp % WPC == ow
         const bool direct = sg.ns == 1;
         const int split = sg.so + ss;
         const bool split_ok = direct || (split >= 0 && split < p.meta.max_splits);
         const size_t rows = (size_t)p.s_q * p.H_q;  // output rows per request: [s_q][H_q]
+        int pass = 0;
 #pragma unroll
-        for (int j = 0; j < NQ; ++j) {
-            if (j >= p.s_q) break;
-            if (j > 0) named_barrier_sync(1, C::NCW * 32);  // the previous pass has read the scratch
-            const float lj0 = warp_sum_xor_4_8_16(l0[j]);
-            const float lj1 = warp_sum_xor_4_8_16(l1[j]);
-            if (lane < 4) {
-                sm_m[warp * C::G + 2 * c4] = m0[j];
-                sm_m[warp * C::G + 2 * c4 + 1] = m1[j];
-                sm_l[warp * C::G + 2 * c4] = lj0;
-                sm_l[warp * C::G + 2 * c4 + 1] = lj1;
-            }
-            float *uw = sm_u + (size_t)warp * C::G * C::UPAD;
+        for (int jl = 0; jl < NQ; ++jl) {
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                // accumulator rows -> head-dim index
-                const int dA = FP8 ? mt * 16 + 2 * r8 : mt * 16 + r8;
-                const int dB = FP8 ? dA + 1 : dA + 8;
-                uw[(2 * c4) * C::UPAD + dA] = acc[mt][j][0];
-                uw[(2 * c4 + 1) * C::UPAD + dA] = acc[mt][j][1];
-                uw[(2 * c4) * C::UPAD + dB] = acc[mt][j][2];
-                uw[(2 * c4 + 1) * C::UPAD + dB] = acc[mt][j][3];
-            }
-            named_barrier_sync(1, C::NCW * 32);
-            if (ctid < C::G) {
-                const int g = ctid;
-                float M = -INFINITY;
-                for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, sm_m[w * C::G + g]);
-                float Ls = 0.f;
-                for (int w = 0; w < C::NCW; ++w) {
-                    const float mw = sm_m[w * C::G + g];
-                    const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-                    sm_w[w * C::G + g] = wt;
-                    Ls += wt * sm_l[w * C::G + g];
+            for (int ow = 0; ow < WPC; ++ow) {
+                const int jj = ow * NQ + jl;
+                if (jj >= p.s_q) continue;
+                if (pass++ > 0) named_barrier_sync(1, C::NCW * 32);  // the previous pass has read the scratch
+                if (warp % WPC == ow) {
+                    const float lj0 = warp_sum_xor_4_8_16(l0[jl]);
+                    const float lj1 = warp_sum_xor_4_8_16(l1[jl]);
+                    if (lane < 4) {
+                        sm_m[warp * C::G + 2 * c4] = m0[jl];
+                        sm_m[warp * C::G + 2 * c4 + 1] = m1[jl];
+                        sm_l[warp * C::G + 2 * c4] = lj0;
+                        sm_l[warp * C::G + 2 * c4 + 1] = lj1;
+                    }
+                    float *uw = sm_u + (size_t)warp * C::G * C::UPAD;
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt) {
+                        // accumulator rows -> head-dim index
+                        const int dA = FP8 ? mt * 16 + 2 * r8 : mt * 16 + r8;
+                        const int dB = FP8 ? dA + 1 : dA + 8;
+                        uw[(2 * c4) * C::UPAD + dA] = acc[mt][jl][0];
+                        uw[(2 * c4 + 1) * C::UPAD + dA] = acc[mt][jl][1];
+                        uw[(2 * c4) * C::UPAD + dB] = acc[mt][jl][2];
+                        uw[(2 * c4 + 1) * C::UPAD + dB] = acc[mt][jl][3];
+                    }
                 }
-                sm_fin[g] = Ls;
-                // lse over the tokens; a request with a single split gets its
-                // attention sink here (the combine adds it to the others)
-                float lse_v = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -INFINITY, fac = 1.f;
-                if (direct && p.sinks != nullptr) {
-                    const float tot = log_add_exp(lse_v, p.sinks[h * C::G + g]);
-                    fac = (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
-                    lse_v = tot;
+                named_barrier_sync(1, C::NCW * 32);
+                if (ctid < C::G) {
+                    const int g = ctid;
+                    float M = -INFINITY;
+                    for (int w = ow; w < C::NCW; w += WPC) M = fmaxf(M, sm_m[w * C::G + g]);
+                    float Ls = 0.f;
+                    for (int w = ow; w < C::NCW; w += WPC) {
+                        const float mw = sm_m[w * C::G + g];
+                        const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                        sm_w[w * C::G + g] = wt;
+                        Ls += wt * sm_l[w * C::G + g];
+                    }
+                    sm_fin[g] = Ls;
+                    // lse over the tokens; a request with a single split gets its
+                    // attention sink here (the combine adds it to the others)
+                    float lse_v = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -INFINITY, fac = 1.f;
+                    if (direct && p.sinks != nullptr) {
+                        const float tot = log_add_exp(lse_v, p.sinks[h * C::G + g]);
+                        fac = (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
+                        lse_v = tot;
+                    }
+                    sm_fin[C::G + g] = fac;
+                    sm_fin[2 * C::G + g] = lse_v;
                 }
-                sm_fin[C::G + g] = fac;
-                sm_fin[2 * C::G + g] = lse_v;
-            }
-            named_barrier_sync(1, C::NCW * 32);
-            const size_t row0 = (size_t)j * p.H_q + (size_t)h * C::G;  // row of head g = row0 + g
-            for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
-                const int g = idx / D, d = idx % D;
-                float u = 0.f;
+                named_barrier_sync(1, C::NCW * 32);
+                const size_t row0 = (size_t)jj * p.H_q + (size_t)h * C::G;  // row of head g = row0 + g
+                for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
+                    const int g = idx / D, d = idx % D;
+                    float u = 0.f;
 #pragma unroll
-                for (int w = 0; w < C::NCW; ++w) u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
-                const float Ls = sm_fin[g];
-                const float o = (Ls > 0.f) ? (u / Ls) * vscale * sm_fin[C::G + g] : 0.f;
-                if (direct)
-                    reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * rows + row0 + g) * D + d] =
-                        __float2bfloat16_rn(o);
-                else if (split_ok)
-                    p.meta.o_part[((size_t)split * rows + row0 + g) * D + d] = o;
-            }
-            if (ctid < C::G) {
-                const int g = ctid;
-                const float v = sm_fin[2 * C::G + g];
-                if (direct)
-                    p.lse[(size_t)sb * rows + row0 + g] = v;
-                else if (split_ok)
-                    p.meta.lse_part[(size_t)split * rows + row0 + g] = v;
+                    for (int w = ow; w < C::NCW; w += WPC)
+                        u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
+                    const float Ls = sm_fin[g];
+                    const float o = (Ls > 0.f) ? (u / Ls) * vscale * sm_fin[C::G + g] : 0.f;
+                    if (direct)
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * rows + row0 + g) * D + d] =
+                            __float2bfloat16_rn(o);
+                    else if (split_ok)
+                        p.meta.o_part[((size_t)split * rows + row0 + g) * D + d] = o;
+                }
+                if (ctid < C::G) {
+                    const int g = ctid;
+                    const float v = sm_fin[2 * C::G + g];
+                    if (direct)
+                        p.lse[(size_t)sb * rows + row0 + g] = v;
+                    else if (split_ok)
+                        p.meta.lse_part[(size_t)split * rows + row0 + g] = v;
+                }
             }
         }
         if (named_barrier_or(1, C::NCW * 32, *abort_flag != 0)) break;
     }
 }
 
-template <int D, bool FP8, int NQ, bool WIN>
+template <int D, bool FP8, int NQ, int WPC, bool WIN>
 static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p, cudaStream_t stream,
                               bool pdl) {
-    using C = GqaCfg<D, FP8, NQ>;
-    auto kern = gqa_decode_kernel<D, FP8, NQ, WIN>;
+    using C = GqaCfg<D, FP8, NQ, WPC>;
+    auto kern = gqa_decode_kernel<D, FP8, NQ, WPC, WIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -597,21 +612,24 @@ static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, con
 
 cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p,
                        cudaStream_t stream, bool pdl) {
-    // one token without a window: the lean build; every other shape carries the window logic
+    // one token without a window: the lean build; every other shape carries the
+    // window logic. Three or four query tokens: a pair of warps per chunk, two each.
     if (p.s_q == 1 && p.window == 0) {
-        if (!fp8 && D == 64) return launch_one<64, false, 1, false>(tkv, tv, p, stream, pdl);
-        if (!fp8 && D == 128) return launch_one<128, false, 1, false>(tkv, tv, p, stream, pdl);
-        if (fp8 && D == 128) return launch_one<128, true, 1, false>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 64) return launch_one<64, false, 1, 1, false>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 1, 1, false>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 1, 1, false>(tkv, tv, p, stream, pdl);
     } else if (p.s_q == 1) {
-        if (!fp8 && D == 64) return launch_one<64, false, 1, true>(tkv, tv, p, stream, pdl);
-        if (!fp8 && D == 128) return launch_one<128, false, 1, true>(tkv, tv, p, stream, pdl);
-        if (fp8 && D == 128) return launch_one<128, true, 1, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 64) return launch_one<64, false, 1, 1, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 1, 1, true>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 1, 1, true>(tkv, tv, p, stream, pdl);
     } else if (p.s_q == 2) {
-        if (!fp8 && D == 64) return launch_one<64, false, 2, true>(tkv, tv, p, stream, pdl);
-        if (!fp8 && D == 128) return launch_one<128, false, 2, true>(tkv, tv, p, stream, pdl);
-        if (fp8 && D == 128) return launch_one<128, true, 2, true>(tkv, tv, p, stream, pdl);
-    } else if (p.s_q <= kMaxSqD64 && !fp8 && D == 64) {
-        return launch_one<64, false, kMaxSqD64, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 64) return launch_one<64, false, 2, 1, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 2, 1, true>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 2, 1, true>(tkv, tv, p, stream, pdl);
+    } else if (p.s_q <= 4) {
+        if (!fp8 && D == 64) return launch_one<64, false, 2, 2, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 128) return launch_one<128, false, 2, 2, true>(tkv, tv, p, stream, pdl);
+        if (fp8 && D == 128) return launch_one<128, true, 2, 2, true>(tkv, tv, p, stream, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -11,7 +11,7 @@ constexpr int kTmaElemBytes = 8;           // element size the pool tensor maps 
 constexpr int32_t kMetaMagic = 0x44414d31;  // "DAM1"
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kMaxSqD64 = 4;               // query tokens per request: bf16 D = 64 kernel
-constexpr int kMaxSqD128 = 2;              // bf16 / e4m3 D = 128 kernels
+constexpr int kMaxSqD128 = 4;              // bf16 / e4m3 D = 128 kernels
 
 // sched_meta header words
 enum MetaHeader : int {

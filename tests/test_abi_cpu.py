@@ -134,9 +134,9 @@ def test_s_q_limits_and_partial_sizes(lib):
     def rc(**kw):
         return lib.decode_attn_sched_meta_bytes(ctypes.byref(_desc(**kw)), ctypes.byref(n))
     assert rc(s_q=0) == 0 and rc(s_q=1) == 0 and rc(s_q=2) == 0
-    assert rc(s_q=3) == -3                                   # D = 128: up to 2 drafts
+    assert rc(s_q=3) == 0 and rc(s_q=4) == 0 and rc(s_q=5) == -3   # up to 4 query tokens
     assert rc(D_qk=64, D_v=64, s_q=4) == 0 and rc(D_qk=64, D_v=64, s_q=5) == -3
-    assert rc(kv_dtype=da.KV_FP8, s_q=2) == 0 and rc(kv_dtype=da.KV_FP8, s_q=3) == -3
+    assert rc(kv_dtype=da.KV_FP8, s_q=4) == 0 and rc(kv_dtype=da.KV_FP8, s_q=5) == -3
     assert rc(s_q=-1) == -2
     # the split partials hold one row per (draft, query head)
     o1, o2 = da.meta_offsets(_desc()), da.meta_offsets(_desc(s_q=2))

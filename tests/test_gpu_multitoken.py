@@ -45,6 +45,11 @@ CASES = [
     (KV_BF16, 128, 2, 32, 4),
     (KV_FP8, 128, 2, 16, 0),
     (KV_FP8, 128, 2, 64, 1),
+    # three or four query tokens at D = 128: a pair of warps per chunk
+    (KV_BF16, 128, 3, 16, 0),
+    (KV_BF16, 128, 4, 64, 2),
+    (KV_FP8, 128, 4, 32, 0),
+    (KV_FP8, 128, 3, 8, 3),
 ]
 
 
@@ -83,7 +88,7 @@ def test_last_draft_matches_single_token_kernel():
     assert (lse[:, -1] - l1).abs().max().item() <= LSE_TOL
 
 
-@pytest.mark.parametrize("name", ["spec2_gqa_bf16", "spec4_gqa_d64", "spec2_fp8_gqa"])
+@pytest.mark.parametrize("name", ["spec2_gqa_bf16", "spec4_gqa_d64", "spec2_fp8_gqa", "spec4_gqa_bf16"])
 def test_multitoken_bench_workloads_sampled(name):
     """The benchmark's multi-token workloads at full size, in its launch
     configuration; the oracle checks a sample of (request, KV head) units."""
@@ -103,6 +108,6 @@ def test_multitoken_bench_workloads_sampled(name):
 def test_unsupported_s_q_rejected_on_host():
     ensure_built()
     d = da.Desc.make(B=2, H_kv=2, G=8, D_qk=128, D_v=128, page_size=16, max_pages_per_seq=4, num_pages=10,
-                     s_q=3)
+                     s_q=5)
     with pytest.raises(da.DecodeAttnError):
         da.sched_meta_bytes(d)

@@ -3,14 +3,16 @@
 kernels read; the ordered lists must equal the reference built from the
 oracle's partition and the block table: for each work unit (part, KV head),
 chunk by chunk, the rows its boxes (GQA: one TMA box of min(P, 64) tokens;
-MLA: one token) must read, and -2 where a box lies past the sequence."""
+MLA: one token) must read, and -2 where a box lies past the sequence (or,
+with a sliding window, wholly before it; with sparse decode, where a slot
+lists no valid position)."""
 import ctypes
 
 import pytest
 import torch
 
 import paged_kv_cache_60_gb300 as da
-from oracle.sched_ref import CHUNK, part_segments, sched_ref
+from oracle.sched_ref import CHUNK, first_chunk, part_segments, sched_ref, window_start
 from workloads import KV_BF16, KV_FP8, KV_MLA656, WorkloadSpec, make_workload
 
 from gpu_util import DeviceWorkload, device_sms, make_desc, debug_build_library
@@ -36,7 +38,7 @@ def _reference(w, ref, rows_per_chunk, row_of):
         for (b, _split, lc0, lc1) in part_segments(ref, p):
             L = w.lengths[b]
             for lc in range(lc0, lc1):
-                chunks.append([row_of(bt[b], L, lc, j) for j in range(rows_per_chunk)])
+                chunks.append([row_of(bt[b], L, lc, j, b) for j in range(rows_per_chunk)])
         parts.append(chunks)
     return parts
 
@@ -46,13 +48,13 @@ def _run(tlib, w, desc, units, cap, per_chunk):
     s = w.spec
     trace = torch.full((units, cap, per_chunk), FILL, dtype=torch.int32, device="cuda")
     meta = torch.empty(da.sched_meta_bytes(desc), dtype=torch.uint8, device="cuda")
-    out = torch.empty(s.B, s.H_q, s.D_v, dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(s.B, s.H_q, dtype=torch.float32, device="cuda")
+    out = torch.empty(s.B, s.s_q * s.H_q, s.D_v, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(s.B, s.s_q * s.H_q, dtype=torch.float32, device="cuda")
     assert tlib.decode_attn_debug_page_trace(ctypes.c_void_p(trace.data_ptr()), cap) == 0
     try:
         da.sched_meta(desc, dw.cache_seqlens, meta, lib=tlib)
         da.fwd(desc, dw.q, dw.k_pool, dw.v_pool, dw.k_scale, dw.v_scale, dw.block_table, dw.cache_seqlens,
-               meta, out, lse, lib=tlib)
+               meta, out, lse, sinks=dw.sinks, indices=dw.indices, lib=tlib)
         torch.cuda.synchronize()
     finally:
         tlib.decode_attn_debug_page_trace(None, 0)
@@ -84,6 +86,11 @@ GQA_CASES = [
     (dict(page_size=64, lengths=[700, 70, 7, 1300, 0, 64]), 6),
     (dict(page_size=8, lengths=[129, 64, 65], splits=3), 0),
     (dict(page_size=128, lengths=[1000, 130]), 0),
+    # sliding windows: the pages before each window are never read
+    (dict(page_size=16, lengths=[517, 1, 300, 64, 65], window=100), 0),
+    (dict(page_size=8, lengths=[1000, 129], window=37, splits=2), 0),
+    (dict(page_size=256, lengths=[1536, 300], window=700, sinks=True), 0),
+    (dict(D_qk=64, D_v=64, page_size=32, lengths=[900, 3, 70], window=64, s_q=3), 0),
 ]
 
 
@@ -93,14 +100,20 @@ def test_gqa_page_trace_bit_exact(tlib, case):
     w = make_workload(_gqa(**kw))
     s = w.spec
     desc = make_desc(w, num_sms=nsm)
-    ref = sched_ref(w.lengths, s.H_kv, s.splits, nsm or device_sms())
+    ref = sched_ref(w.lengths, s.H_kv, s.splits, nsm or device_sms(), window=s.window, s_q=s.s_q)
     P = s.page_size
     bt_tok = min(P, CHUNK)
     nb = CHUNK // bt_tok
 
-    def row_of(bt_row, L, lc, j):
-        tok = lc * CHUNK + j * bt_tok
-        return bt_row[tok // P] * P + (tok % P if P > CHUNK else 0) if tok < L else -2
+    def row_of(bt_row, L, lc, j, b):
+        # local chunk lc is the request's chunk fc + lc; boxes wholly before the
+        # window (or past the sequence) are not read
+        fc = first_chunk(L, s.window, s.s_q)
+        start = window_start(L, s.window, s.s_q)
+        tok = (fc + lc) * CHUNK + j * bt_tok
+        if tok >= L or tok + bt_tok <= start:
+            return -2
+        return bt_row[tok // P] * P + (tok % P if P > CHUNK else 0)
 
     per_part = _reference(w, ref, nb, row_of)
     cap = max(1, max(len(c) for c in per_part))
@@ -113,6 +126,9 @@ MLA_CASES = [
     dict(),
     dict(page_size=16, splits=3),
     dict(page_size=32, lengths=[2500, 90, 0, 64]),
+    # sparse top-k: the rows of the listed positions, slot by slot
+    dict(page_size=16, lengths=[2500, 90, 0, 64], topk=200),
+    dict(page_size=64, lengths=[5000, 3000, 10], topk=130, splits=2),
 ]
 
 
@@ -126,11 +142,14 @@ def test_mla_page_trace_bit_exact(tlib, case):
     s = w.spec
     desc = make_desc(w)
     nsm = device_sms() if s.splits else 2 * da.num_parts(desc)
-    ref = sched_ref(w.lengths, 1, s.splits, nsm, cpc=2)
+    ref = sched_ref(w.lengths, 1, s.splits, nsm, cpc=2, topk=s.topk)
     P = s.page_size
 
-    def row_of(bt_row, L, lc, j):
+    def row_of(bt_row, L, lc, j, b):
         t = lc * CHUNK + j
+        if s.topk > 0:   # sparse: the position listed in slot t, if valid
+            t = int(w.indices[b, t]) if t < s.topk else -1
+            return bt_row[t // P] * P + t % P if 0 <= t < L else -2
         return bt_row[t // P] * P + t % P if t < L else -2
 
     per_part = _reference(w, ref, CHUNK, row_of)

@@ -86,6 +86,10 @@ CONFIGS = [
         name="spec4_gqa_d64", B=32, H_kv=8, G=8, D_qk=64, D_v=64, page_size=64,
         length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1007, s_q=4,
         description="B=32 s_q=4 H_q=64 H_kv=8 D=64 P=64 L~U[1024,8192] auto splits, draft chain of 4"),
+    WorkloadSpec(
+        name="spec4_gqa_bf16", B=32, H_kv=8, G=8, D_qk=128, D_v=128, page_size=64,
+        length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1010, s_q=4,
+        description="B=32 s_q=4 H_q=64 H_kv=8 D=128 P=64 L~U[1024,8192] auto splits, draft chain of 4"),
     # sliding window and attention sinks (the pages name both; no measured shape)
     WorkloadSpec(
         name="window_sinks_gqa_bf16", B=32, H_kv=8, G=8, D_qk=128, D_v=128, page_size=64,
