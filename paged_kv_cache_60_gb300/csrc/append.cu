@@ -19,9 +19,11 @@
 // or [num_pages][page_size][1][656].
 //
 // The work is a scatter of a few hundred bytes per request, HBM / latency
-// bound: one 16-byte load and one 16- or 8-byte store per thread, coalesced
-// along the token's contiguous H_kv * D values; the latent format takes one
-// warp per token (lanes 8k..8k+7 own block k and reduce its max with shuffles).
+// bound: per thread the same 16-byte vector of K and of V (two loads, two
+// 16- or 8-byte stores), coalesced along the token's contiguous H_kv * D
+// values; the latent format takes one warp per token (lanes 8k..8k+7 own
+// block k and reduce its max with shuffles). Every request's new row is read,
+// even when its position skips it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -97,32 +99,33 @@ __device__ __forceinline__ int64_t slot_of(const AppendParams &p, int b, bool re
     return (int64_t)page * p.page_size + t % p.page_size;
 }
 
-// bf16 / e4m3 pools. Work item = one 16-byte vector of 8 values of K or V of
-// one request; items of one request are consecutive (K vectors, then V).
+// bf16 / e4m3 pools. Work item = one 16-byte vector of 8 values at the same
+// place in K and in V of one request (items of a request are consecutive).
+// The two row loads are issued before the position and page lookups, so the
+// three latencies overlap.
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads) append_gqa_kernel(const AppendParams p) {
     pdl_wait();               // positions, block table and new rows may come from the previous kernel
     pdl_launch_dependents();  // the next kernel waits for this grid before it reads the pool
     const int vpr = p.D >> 3;
-    const int per_tensor = p.H_kv * vpr;
-    const int64_t per_req = 2 * (int64_t)per_tensor;
+    const int per_req = p.H_kv * vpr;
     const int64_t total = (int64_t)p.B * per_req;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
         const int b = (int)(i / per_req);
-        const int r = (int)(i - (int64_t)b * per_req);
-        const int64_t slot = slot_of(p, b, r == 0);
+        const int e = (int)(i - (int64_t)b * per_req);
+        const int64_t src = (int64_t)b * p.row_stride + (int64_t)e * 8;
+        const uint4 xk = ld_stream_v4(p.k_new + src);
+        const uint4 xv = ld_stream_v4(p.v_new + src);
+        const int64_t slot = slot_of(p, b, e == 0);
         if (slot < 0) continue;
-        const bool is_v = r >= per_tensor;
-        const int e = is_v ? r - per_tensor : r;
-        const uint16_t *src = (is_v ? p.v_new : p.k_new) + (int64_t)b * p.row_stride + (int64_t)e * 8;
-        const uint4 x = ld_stream_v4(src);
-        uint8_t *pool = is_v ? p.v_pool : p.k_pool;
-        const int64_t vec = slot * per_tensor + e;
+        const int64_t vec = slot * per_req + e;
         if constexpr (!kFp8) {
-            st_v4(pool + vec * 16, x);
+            st_v4(p.k_pool + vec * 16, xk);
+            st_v4(p.v_pool + vec * 16, xv);
         } else {
-            const float s = __ldg((is_v ? p.v_scale : p.k_scale) + e / vpr);
-            st_v2(pool + vec * 8, quant8(x, s));
+            const int h = e / vpr;
+            st_v2(p.k_pool + vec * 8, quant8(xk, __ldg(p.k_scale + h)));
+            st_v2(p.v_pool + vec * 8, quant8(xv, __ldg(p.v_scale + h)));
         }
     }
 }
@@ -135,11 +138,13 @@ __global__ void __launch_bounds__(kThreads) append_mla_kernel(const AppendParams
     const int lane = threadIdx.x & 31;
     constexpr int kWarps = kThreads / 32;
     for (int b = blockIdx.x * kWarps + (threadIdx.x >> 5); b < p.B; b += gridDim.x * kWarps) {
-        const int64_t slot = slot_of(p, b, lane == 0);   // uniform over the warp
-        if (slot < 0) continue;
+        // the row loads first, then the position and page lookups
         const uint16_t *src = p.k_new + (int64_t)b * p.row_stride;
         const uint4 a0 = ld_stream_v4(src + lane * 16);
         const uint4 a1 = ld_stream_v4(src + lane * 16 + 8);
+        const uint4 rope = lane < 8 ? ld_stream_v4(src + kLatentNope + lane * 8) : make_uint4(0u, 0u, 0u, 0u);
+        const int64_t slot = slot_of(p, b, lane == 0);   // uniform over the warp
+        if (slot < 0) continue;
         const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         // max |x| by the magnitude bits: exact, and a NaN wins (scale 1 then)
         uint32_t m = 0;
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) append_mla_kernel(const AppendParams
         if (lane == 0)
             st_v4(row + kLatentScales,
                   make_uint4(__float_as_uint(scale), __float_as_uint(s1), __float_as_uint(s2), __float_as_uint(s3)));
-        if (lane < 8) st_v4(row + kLatentRope + lane * 16, ld_stream_v4(src + kLatentNope + lane * 8));
+        if (lane < 8) st_v4(row + kLatentRope + lane * 16, rope);
     }
 }
 
@@ -184,13 +189,13 @@ cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    constexpr int64_t kMaxBlocks = 152 * 16;   // grid-stride beyond 16 CTAs per SM
+    constexpr int64_t kMaxBlocks = 1 << 20;    // grid-stride beyond that
     if (kv_dtype == DA_KV_FP8_MLA656) {
         const int64_t blocks = (p.B + kThreads / 32 - 1) / (kThreads / 32);
         cfg.gridDim = dim3((unsigned)(blocks < kMaxBlocks ? blocks : kMaxBlocks));
         return cudaLaunchKernelEx(&cfg, append_mla_kernel, p);
     }
-    const int64_t items = (int64_t)p.B * 2 * p.H_kv * (p.D / 8);
+    const int64_t items = (int64_t)p.B * p.H_kv * (p.D / 8);
     const int64_t blocks = (items + kThreads - 1) / kThreads;
     cfg.gridDim = dim3((unsigned)(blocks < kMaxBlocks ? blocks : kMaxBlocks));
     if (kv_dtype == DA_KV_FP8_PER_TENSOR) return cudaLaunchKernelEx(&cfg, append_gqa_kernel<true>, p);
