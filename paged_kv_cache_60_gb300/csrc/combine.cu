@@ -20,17 +20,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DV>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
-    pdl_wait();
-    pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid before reading
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hq = blockIdx.y * 4 + warp;
-    // independent loads first, then the checks
+    // The scheduling words come from the metadata kernel, which completed
+    // before the split-KV kernel passed its own wait (and so before this grid
+    // could start): read them from L2 ahead of the wait, so that their latency
+    // overlaps the split-KV kernel's tail. The partials need the wait.
     const int32_t *hd = p.meta.header;
-    const int ns = p.meta.num_splits[b];
-    const int so = p.meta.split_offset[b];
-    if (!meta_header_ok(load_meta_header(hd), p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q, p.window,
-                        p.topk))
+    const int ns = __ldcg(p.meta.num_splits + b);
+    const int so = __ldcg(p.meta.split_offset + b);
+    const MetaHdr mh = load_meta_header_cg(hd);
+    pdl_wait();
+    pdl_launch_dependents();  // the next kernel may start its prologue; it waits for this grid before reading
+    if (!meta_header_ok(mh, p.B, p.H_kv, p.G, p.splits, p.num_parts, p.s_q, p.window, p.topk))
         return;  // the split-KV kernel has flagged the mismatch
     if (hq >= p.rows) return;
     if (ns == 1) return;  // written directly by the split-KV kernel

@@ -37,6 +37,11 @@ __device__ __forceinline__ MetaHdr load_meta_header(const int32_t *hd) {
     const int4 *v = reinterpret_cast<const int4 *>(hd);
     return MetaHdr{v[0], v[1], v[3], v[4]};
 }
+// the same words through L2 only (no L1 line from an earlier grid can answer)
+__device__ __forceinline__ MetaHdr load_meta_header_cg(const int32_t *hd) {
+    const int4 *v = reinterpret_cast<const int4 *>(hd);
+    return MetaHdr{__ldcg(v), __ldcg(v + 1), __ldcg(v + 3), __ldcg(v + 4)};
+}
 // magic, B, H_kv, G, splits, num_parts, s_q, window, topk all as expected
 __device__ __forceinline__ bool meta_header_ok(const MetaHdr &h, int B, int H_kv, int G, int splits, int num_parts,
                                                int s_q, int window, int topk) {
