@@ -278,7 +278,13 @@ def oracle_time_per_call(w, budget_s):
     else:
         attend = oracle.attend
     units_all = [(b, h) for b in range(s.B) for h in range(s.H_kv)]
-    cost = {u: (min(w.lengths[u[0]], s.topk) if s.topk > 0 else w.lengths[u[0]]) for u in units_all}
+    def unit_cost(L):   # tokens one (request, KV head) unit reads
+        if s.topk > 0:
+            return min(L, s.topk)
+        if s.window > 0:
+            return min(L, s.window + s.s_q - 1)
+        return L
+    cost = {u: unit_cost(w.lengths[u[0]]) for u in units_all}
     total_cost = sum(cost.values())
     # cheap probe on the shortest unit to size the sample
     probe = min(units_all, key=lambda u: cost[u])

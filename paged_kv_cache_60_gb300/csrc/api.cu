@@ -421,7 +421,8 @@ int decode_attn_append_kv(const da_desc *desc, const void *k_new, const void *v_
     if (!desc) return DA_ERR_NULL;
     const da_desc *d = desc;
     if (d->B < 1 || d->B > (1 << 24) || d->H_kv < 1 || d->H_kv > 4096 || d->page_size < 1 ||
-        d->max_pages_per_seq < 1 || d->num_pages < 1 || d->D_qk < 1 || d->D_v < 1)
+        d->max_pages_per_seq < 1 || d->num_pages < 1 || d->D_qk < 1 || d->D_v < 1 || d->D_qk > 4096 ||
+        d->D_v > 4096)
         return DA_ERR_DIMS;
     if ((int64_t)d->max_pages_per_seq * d->page_size > (int64_t)INT32_MAX) return DA_ERR_DIMS;
     if ((int64_t)d->B * d->max_pages_per_seq > (int64_t)INT32_MAX) return DA_ERR_DIMS;
