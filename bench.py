@@ -364,7 +364,8 @@ def run_ours(args, rank, world, local):
     # metadata built once beforehand and reused, as every layer of a decode
     # step reuses it; decode_attn_sched_meta is timed on its own and together
     # with the call (sched_meta_us, with_sched_meta_us).
-    launches_per_step = 2
+    # split-KV kernel + combine; a fixed split count of 2..8 merges inside the split-KV kernel
+    launches_per_step = 1 if (spec.kv_dtype != da.KV_MLA656 and 2 <= spec.splits <= 8) else 2
 
     # ---- CUDA graphs of several calls each (calls rotate over the input
     # copies, so consecutive calls read different memory), or eager launches.

@@ -345,6 +345,9 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.s_q = sq_of(desc);
         p.window = desc->window;
         p.sinks = sinks;
+        // a fixed split count of 2..8: the splits of a (request, KV head) merge
+        // inside one thread-block cluster and no combine kernel runs
+        p.cluster_merge = (desc->splits >= 2 && desc->splits <= 8) ? 1 : 0;
         p.max_pages = desc->max_pages_per_seq;
         p.num_pages = desc->num_pages;
         p.page_size = P;
@@ -388,6 +391,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     }
     if (opts && opts->main_end && cudaEventRecord(opts->main_end, stream) != cudaSuccess) return DA_ERR_CUDA;
+    if (!mla && desc->splits >= 2 && desc->splits <= 8) return DA_OK;  // merged in the split-KV kernel
     CombineParams c;
     c.meta = mv;
     c.out = out;

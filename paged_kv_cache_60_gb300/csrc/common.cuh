@@ -353,7 +353,21 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
 
+// Split cluster barrier: arrive (releasing this thread's earlier writes, e.g.
+// mbarrier inits) now, wait (until every non-exited thread of the cluster has
+// arrived) later, so that the time in between overlaps other work.
+__device__ __forceinline__ void cluster_arrive_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Every thread of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");

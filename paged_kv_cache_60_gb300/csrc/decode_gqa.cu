@@ -84,12 +84,92 @@ struct GqaCfg {
     static constexpr int OFF_W = OFF_L + NCW * G * 4;
     static constexpr int OFF_FIN = OFF_W + NCW * G * 4;
     static constexpr int OFF_BAR = (OFF_FIN + 4 * G * 4 + 7) / 8 * 8;
-    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8 + 16;  // + the cluster merge's two barriers
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
     static constexpr int MIN_BLOCKS = (D == 64 && !FP8 && NQ == 1 && WPC == 1) ? 2 : 1;
     static_assert(ROW % 128 == 0, "rows must be whole 128-byte boxes");
     static_assert(!FP8 || NX == 1, "fp8 path expects one 128-byte box per row");
 };
+
+// Split merge inside a cluster (fixed split count S <= 8): the S CTAs of a
+// (request, KV head) form one thread-block cluster; each has left its split's
+// normalised partial (o, lse) for every row in its own shared memory. Once
+// all S have signalled, CTA rank r merges dims [floor(r D / S),
+// floor((r + 1) D / S)) of every row by the rule of the combine kernel
+// (lse = M + ln sum e^(lse_s - M), out = sum e^(lse_s - lse) o_s, splits in
+// index order), adds the attention
+// sink and writes out and lse. It then waits until every split has finished
+// reading its memory before it exits. Called by the consumer warps only.
+template <int D>
+__device__ __forceinline__ void cluster_merge(const GqaParams &p, float *xo, float *xl, uint64_t *xready,
+                                              uint64_t *xdone, const volatile int *never, int b, int h,
+                                              bool aborted) {
+    constexpr int G = 8;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const int nthr = blockDim.x - 32;  // consumer threads
+    const int ctid = threadIdx.x;
+    const int S = p.splits;
+    const int rows_cta = p.s_q * G;
+    if (aborted || b < 0) {
+        // no valid partial: weight 0 for every row
+        for (int r = ctid; r < rows_cta; r += nthr) xl[r] = -INFINITY;
+    }
+    named_barrier_sync(1, nthr);
+    cluster_wait_all();  // the other splits' barriers are initialised (their threads arrived at start)
+    if (ctid == 0) {
+        fence_acq_rel_cluster();  // this CTA's partial, before the arrivals below release it
+        for (int q = 0; q < S; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(xready), (uint32_t)q));
+    }
+    const int lane = ctid & 31;
+    bool ok = mbar_wait_warp_cluster(xready, 0, never, p.wait_limit_ns);
+    ok = !named_barrier_or(1, nthr, !ok);  // every consumer warp saw all S arrivals
+    if (!ok) {
+        if (ctid == 0) atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
+    } else if (b >= 0) {
+        const uint32_t rank = cluster_ctarank();
+        const int d0 = (int)rank * D / S, dpc = ((int)rank + 1) * D / S - d0;  // this CTA's dims
+        const uint32_t xo_s = smem_u32(xo), xl_s = smem_u32(xl);
+        const size_t rows = (size_t)p.s_q * p.H_q;
+        for (int idx = ctid; idx < rows_cta * dpc; idx += nthr) {
+            const int r = idx / dpc, d = d0 + idx % dpc;
+            float ls[8];
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                ls[q] = q < S ? ld_cluster_f32(mapa_shared(xl_s + 4u * r, (uint32_t)q)) : -INFINITY;
+                M = fmaxf(M, ls[q]);
+            }
+            float acc = 0.f, lse_v = -INFINITY;
+            if (M != -INFINITY) {
+                float Z = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) Z += ls[q] == -INFINITY ? 0.f : ex2((ls[q] - M) * kLog2e);
+                lse_v = M + logf(Z);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (ls[q] == -INFINITY) continue;  // empty split, or a slot past S
+                    const float w = ex2((ls[q] - lse_v) * kLog2e);
+                    acc += w * ld_cluster_f32(mapa_shared(xo_s + 4u * ((uint32_t)r * D + d), (uint32_t)q));
+                }
+            }
+            const int jj = r / G, g = r % G;
+            if (p.sinks != nullptr) {
+                const float tot = log_add_exp(lse_v, p.sinks[h * G + g]);
+                acc *= (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
+                lse_v = tot;
+            }
+            const size_t orow = (size_t)b * rows + (size_t)jj * p.H_q + (size_t)h * G + g;
+            reinterpret_cast<__nv_bfloat16 *>(p.out)[orow * D + d] = __float2bfloat16_rn(acc);
+            if (rank == 0 && idx % dpc == 0) p.lse[orow] = lse_v;
+        }
+    }
+    // this CTA's loads from the others are done: tell them, then wait until they are done with ours
+    named_barrier_sync(1, nthr);
+    if (ctid == 0)
+        for (int q = 0; q < S; ++q) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(xdone), (uint32_t)q));
+    if (!mbar_wait_warp_cluster(xdone, 0, never, p.wait_limit_ns) && lane == 0)
+        atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
+}
 
 // NQ x WPC: query tokens per request the kernel is compiled for (s_q <=
 // NQ * WPC; warp w of a chunk's group holds tokens [(w % WPC) NQ, (w % WPC + 1)
@@ -110,6 +190,10 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *empty = full + C::NS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
+    // cluster merge: partials of every split ready / read by every split; waits
+    // on them ignore the abort flag (a word that stays 0)
+    uint64_t *xready = empty + C::NS, *xdone = xready + 1;
+    const volatile int *never = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int part = blockIdx.x, h = blockIdx.y;
@@ -120,6 +204,11 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
             mbar_init(&empty[i], WPC);  // every warp of the chunk's group
         }
         *abort_flag = 0;
+        abort_flag[1] = 0;
+        if (p.cluster_merge) {
+            mbar_init(xready, p.splits);  // one arrival from each split of the request
+            mbar_init(xdone, p.splits);
+        }
 #ifdef DA_PAGE_TRACE
         mbar_init(reinterpret_cast<uint64_t *>(smem + C::OFF_FLAG + 8), 1);  // never arrived at
 #endif
@@ -131,6 +220,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         if (!p.kv_combined) prefetch_tmap(&tm_v);
     }
     __syncthreads();
+    // every split's merge barriers exist before any remote arrival: arrive here,
+    // wait (consumer threads) just before the merge's first remote arrival
+    if (p.cluster_merge) cluster_arrive_all();
     pdl_wait();
     pdl_launch_dependents();
 
@@ -267,8 +359,14 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
     SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
     int i = 0;
     Seg sg;
+    int merge_b = -1;  // cluster merge: the request of this CTA's (single) segment
+    // cluster merge: this split's normalised partial [rows][D] and lse [rows],
+    // rows = s_q * G, in the stage memory (idle once the segment is done)
+    float *xo = reinterpret_cast<float *>(smem);
+    float *xl = xo + (size_t)p.s_q * C::G * D;
     while (wk.next(sg)) {
         const int sb = sg.b, ss = sg.s, lc0 = sg.lc0, lc1 = sg.lc1, L = sg.L;
+        merge_b = sb;
         // query fragments (B operand, n = query head r8 of this group), one
         // n8 tile per query token of the request; q is [B][s_q][H_q][D]
         uint32_t qf[C::KS][NQ][2];
@@ -573,6 +671,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                     if (direct)
                         reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * rows + row0 + g) * D + d] =
                             __float2bfloat16_rn(o);
+                    else if (p.cluster_merge)
+                        xo[(size_t)(jj * C::G + g) * D + d] = o;
                     else if (split_ok)
                         p.meta.o_part[((size_t)split * rows + row0 + g) * D + d] = o;
                 }
@@ -581,6 +681,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                     const float v = sm_fin[2 * C::G + g];
                     if (direct)
                         p.lse[(size_t)sb * rows + row0 + g] = v;
+                    else if (p.cluster_merge)
+                        xl[jj * C::G + g] = v;
                     else if (split_ok)
                         p.meta.lse_part[(size_t)split * rows + row0 + g] = v;
                 }
@@ -588,6 +690,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         }
         if (named_barrier_or(1, C::NCW * 32, *abort_flag != 0)) break;
     }
+    if (p.cluster_merge) cluster_merge<D>(p, xo, xl, xready, xdone, never, merge_b, h, *abort_flag != 0);
 }
 
 template <int D, bool FP8, int NQ, int WPC, bool WIN>
@@ -602,11 +705,22 @@ static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, con
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (p.cluster_merge) {  // the splits of one (request, KV head) as one cluster
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.splits;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, tkv, tv, p);
 }
 
