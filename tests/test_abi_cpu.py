@@ -143,3 +143,35 @@ def test_s_q_limits_and_partial_sizes(lib):
     assert o1[:6] == o2[:6]
     assert (o2[6] - o2[5]) >= 2 * (o1[6] - o1[5]) - 256
     assert (o2[7] - o2[6]) >= 2 * (o1[7] - o1[6]) - 256
+
+
+def test_window_topk_sinks_argument_checks(lib):
+    n = ctypes.c_size_t(0)
+
+    def rc(**kw):
+        return lib.decode_attn_sched_meta_bytes(ctypes.byref(_desc(**kw)), ctypes.byref(n))
+    assert rc(window=-1) == -2
+    assert rc(window=4096) == 0
+    assert rc(topk=64) == -3                       # sparse decode is for the 656-byte format
+    assert rc(topk=-1) == -2
+    # sparse decode without a position list, and sinks with the latent format: refused before launch
+    d = _desc(kv_dtype=da.KV_MLA656, H_kv=1, G=128, D_qk=576, D_v=512, topk=64)
+    if lib.decode_attn_sched_meta_bytes(ctypes.byref(d), ctypes.byref(n)) == 0:
+        P = ctypes.c_void_p
+        g = P(0x10000)
+        opts = da.LaunchOpts(1, None, None, None, None)
+        assert lib.decode_attn_fwd_ex(ctypes.byref(d), g, g, None, None, None, g, g, g, n.value, g, g,
+                                      ctypes.byref(opts), None) == -1
+        dm = _desc(kv_dtype=da.KV_MLA656, H_kv=1, G=128, D_qk=576, D_v=512)
+        nm = ctypes.c_size_t(0)
+        assert lib.decode_attn_sched_meta_bytes(ctypes.byref(dm), ctypes.byref(nm)) == 0
+        opts = da.LaunchOpts(1, None, None, g, None)
+        assert lib.decode_attn_fwd_ex(ctypes.byref(dm), g, g, None, None, None, g, g, g, nm.value, g, g,
+                                      ctypes.byref(opts), None) == -3
+    # misaligned sinks pointer
+    d = _desc()
+    nb = da.sched_meta_bytes(d)
+    g = ctypes.c_void_p(0x10000)
+    opts = da.LaunchOpts(1, None, None, ctypes.c_void_p(0x10002), None)
+    assert lib.decode_attn_fwd_ex(ctypes.byref(d), g, g, g, None, None, g, g, g, nb, g, g, ctypes.byref(opts),
+                                  None) == -4
