@@ -150,7 +150,11 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
 
 /*
  * Decode attention forward. Launches the split-KV kernel and the LSE combine
- * kernel (chained with programmatic dependent launch) on `stream`.
+ * kernel (chained with programmatic dependent launch) on `stream`. With a
+ * fixed split count of 2-8 (desc->splits) and the bf16 or e4m3 formats, the
+ * splits of a (request, KV head) run as one thread-block cluster and merge
+ * their partials through distributed shared memory: the split-KV kernel then
+ * writes out and lse itself and no combine kernel is launched.
  *
  * Several query tokens per request (desc->s_q > 1) verify a chain of draft
  * tokens (XQA page, section "投机解码:XQA 的第二个工作负载", the linear case;
