@@ -132,13 +132,16 @@ __device__ __forceinline__ void cluster_merge(const GqaParams &p, float *xo, flo
         const size_t rows = (size_t)p.s_q * p.H_q;
         for (int idx = ctid; idx < rows_cta * dpc; idx += nthr) {
             const int r = idx / dpc, d = d0 + idx % dpc;
-            float ls[8];
+            // every split's lse and value in one round of loads
+            float ls[8], ov[8];
             float M = -INFINITY;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 ls[q] = q < S ? ld_cluster_f32(mapa_shared(xl_s + 4u * r, (uint32_t)q)) : -INFINITY;
-                M = fmaxf(M, ls[q]);
+                ov[q] = q < S ? ld_cluster_f32(mapa_shared(xo_s + 4u * ((uint32_t)r * D + d), (uint32_t)q)) : 0.f;
             }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) M = fmaxf(M, ls[q]);
             float acc = 0.f, lse_v = -INFINITY;
             if (M != -INFINITY) {
                 float Z = 0.f;
@@ -147,9 +150,8 @@ __device__ __forceinline__ void cluster_merge(const GqaParams &p, float *xo, flo
                 lse_v = M + logf(Z);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    if (ls[q] == -INFINITY) continue;  // empty split, or a slot past S
-                    const float w = ex2((ls[q] - lse_v) * kLog2e);
-                    acc += w * ld_cluster_f32(mapa_shared(xo_s + 4u * ((uint32_t)r * D + d), (uint32_t)q));
+                    if (ls[q] == -INFINITY) continue;  // empty split, or a slot past S (its value unused)
+                    acc += ex2((ls[q] - lse_v) * kLog2e) * ov[q];
                 }
             }
             const int jj = r / G, g = r % G;
