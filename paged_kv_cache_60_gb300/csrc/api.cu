@@ -186,18 +186,32 @@ EncodeTiledFn get_encode_tiled() {
 //   dim 2: KV head (stride = row)           dim 3: global token = page*P + slot (stride row*H_kv)
 //   dim 4: pool, K or V (stride = distance between the two pools)
 // and a box {16, NX, 1, box_tok, 2}: one copy brings one page's K and V rows of
-// one head. base is the lower of the two pools. With pool = nullptr, a 4-D map
-// of one pool (dims 0-3) and a box {16, NX, 1, box_tok}.
+// one head, in shared memory as [pool][token][half][128 B]. base is the lower
+// of the two pools. With pool = nullptr, a 4-D map of one pool (dims 0-3) and
+// a box {16, NX, 1, box_tok}. With half_major the token dimension (1) and the
+// half and head dimensions (2, 3) trade places: the box lands as
+// [pool][half][token][128 B].
 int make_kv_map(CUtensorMap *m, const void *base, uint64_t pool_dist, bool two_pools, const da_desc *d,
-                int elem_bytes, int box_tok) {
+                int elem_bytes, int box_tok, bool half_major) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return DA_ERR_CUDA;
     const cuuint64_t row = (cuuint64_t)d->D_qk * elem_bytes;  // bytes of one token's head
     const cuuint64_t nx = row / 128;
-    cuuint64_t dims[5] = {128 / kTmaElemBytes, nx, (cuuint64_t)d->H_kv,
-                          (cuuint64_t)d->page_size * (cuuint64_t)d->num_pages, 2};
+    const cuuint64_t ntok = (cuuint64_t)d->page_size * (cuuint64_t)d->num_pages;
+    cuuint64_t dims[5] = {128 / kTmaElemBytes, nx, (cuuint64_t)d->H_kv, ntok, 2};
     cuuint64_t strides[4] = {128, row, row * d->H_kv, pool_dist};
     cuuint32_t box[5] = {128 / kTmaElemBytes, (cuuint32_t)nx, 1, (cuuint32_t)box_tok, 2};
+    if (half_major) {  // the token dimension inside the half dimension
+        dims[1] = ntok;
+        dims[2] = nx;
+        dims[3] = (cuuint64_t)d->H_kv;
+        strides[0] = row * d->H_kv;
+        strides[1] = 128;
+        strides[2] = row;
+        box[1] = (cuuint32_t)box_tok;
+        box[2] = (cuuint32_t)nx;
+        box[3] = 1;
+    }
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, two_pools ? 5 : 4, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -321,13 +335,16 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         const uintptr_t ka = reinterpret_cast<uintptr_t>(k_pool), va = reinterpret_cast<uintptr_t>(v_pool);
         const uint64_t dist = ka > va ? (uint64_t)(ka - va) : (uint64_t)(va - ka);
         const bool combined = dist >= pool_bytes && dist < (1ull << 40);
+        // the builds with several query tokens or a window read 256-byte rows half-major
+        const bool half_major = (sq_of(desc) > 1 || desc->window > 0) && desc->D_qk * es > 128;
         CUtensorMap tkv, tv;
         if (combined) {
-            if ((rc = make_kv_map(&tkv, ka < va ? k_pool : v_pool, dist, true, desc, es, box_tok))) return rc;
+            if ((rc = make_kv_map(&tkv, ka < va ? k_pool : v_pool, dist, true, desc, es, box_tok, half_major)))
+                return rc;
             tv = tkv;
         } else {
-            if ((rc = make_kv_map(&tkv, k_pool, 0, false, desc, es, box_tok))) return rc;
-            if ((rc = make_kv_map(&tv, v_pool, 0, false, desc, es, box_tok))) return rc;
+            if ((rc = make_kv_map(&tkv, k_pool, 0, false, desc, es, box_tok, half_major))) return rc;
+            if ((rc = make_kv_map(&tv, v_pool, 0, false, desc, es, box_tok, half_major))) return rc;
         }
         GqaParams p;
         p.q = q;
@@ -348,6 +365,7 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         // a fixed split count of 2..8: the splits of a (request, KV head) merge
         // inside one thread-block cluster and no combine kernel runs
         p.cluster_merge = (desc->splits >= 2 && desc->splits <= 8) ? 1 : 0;
+        p.half_major = half_major ? 1 : 0;
         p.max_pages = desc->max_pages_per_seq;
         p.num_pages = desc->num_pages;
         p.page_size = P;

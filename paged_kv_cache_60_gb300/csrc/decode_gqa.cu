@@ -309,10 +309,18 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                         const int in_page = (P > kChunk) ? (tok % P) : 0;
                         uint8_t *st = smem + (size_t)stage * C::STAGE + lane * box_bytes;
                         if (p.kv_combined) {
-                            tma_load_5d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, 0, pol);
+                            if (p.half_major)
+                                tma_load_5d(st, &tm_kv, &full[stage], 0, pg * P + in_page, 0, h, 0, pol);
+                            else
+                                tma_load_5d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, 0, pol);
                         } else {  // K map in tm_kv, V map in tm_v, same box image
-                            tma_load_4d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, pol);
-                            tma_load_4d(st + box_bytes / 2, &tm_v, &full[stage], 0, 0, h, pg * P + in_page, pol);
+                            if (p.half_major) {
+                                tma_load_4d(st, &tm_kv, &full[stage], 0, pg * P + in_page, 0, h, pol);
+                                tma_load_4d(st + box_bytes / 2, &tm_v, &full[stage], 0, pg * P + in_page, 0, h, pol);
+                            } else {
+                                tma_load_4d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, pol);
+                                tma_load_4d(st + box_bytes / 2, &tm_v, &full[stage], 0, 0, h, pg * P + in_page, pol);
+                            }
                         }
                     }
                     ++i;
@@ -334,17 +342,26 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
     const float kscale = FP8 ? p.k_scale[h] : 1.f;
     const float vscale = FP8 ? p.v_scale[h] : 1.f;
     const float sl2 = p.scale_log2 * kscale;
-    // Stage layout: box j (tokens [j*bt, (j+1)*bt)) at j*box_bytes holds
-    // [first pool][bt tokens][NX halves][128 B], then the same for the second
-    // pool; p.kv_swap tells which pool comes first. With bt >= 8 every box and
-    // half starts on a 1024-byte boundary, so the 128-byte swizzle key of
-    // token t, half x is (t*NX + x) & 7.
+    // Stage layout: box j (tokens [j*bt, (j+1)*bt)) at j*box_bytes holds one
+    // pool's rows, then the other's (p.kv_swap tells which pool comes first).
+    // With bt >= 8 every box and half starts on a 1024-byte boundary. Rows of
+    // 256 bytes (NX = 2) are laid out token-major, [token][half][128 B], in the
+    // lean one-token build: each row is one 256-byte read, and the 128-byte
+    // swizzle key of token t, half x is (2t + x) & 7 (a 2-way bank conflict on
+    // ldmatrix, which that HBM-bound build does not feel); and half-major,
+    // [half][token][128 B], in the builds with several query tokens or a
+    // window, which do more arithmetic per byte: key t & 7, no conflict.
+    // With NX = 1 the two are the same.
+    constexpr bool HM = WIN && C::NX > 1;
     const int bt = p.box_tokens, lbt = p.log2_box_tokens;
-    const uint32_t half_bytes = (uint32_t)bt * C::NX * 128u;
+    const uint32_t half_bytes = (uint32_t)bt * C::NX * 128u;   // one pool's part of a box
+    const uint32_t xstride = HM ? (uint32_t)bt * 128u : 128u;  // half 0 -> half 1 of a row
     const uint32_t k_half = p.kv_swap ? half_bytes : 0u, v_half = p.kv_swap ? 0u : half_bytes;
-    auto row_of = [&](int tok) -> uint32_t {
-        return (uint32_t)((tok >> lbt) * 2 * bt + (tok & (bt - 1))) * (C::NX * 128u);
+    auto row_of = [&](int tok) -> uint32_t {  // half 0 of token tok's row
+        return HM ? (uint32_t)((tok >> lbt) * 2 * bt * C::NX + (tok & (bt - 1))) * 128u
+                  : (uint32_t)((tok >> lbt) * 2 * bt + (tok & (bt - 1))) * (C::NX * 128u);
     };
+    auto key_of = [&](int tok, int x) -> int { return HM ? (tok & 7) : ((tok * C::NX + x) & 7); };
     // tokens this lane addresses in ldmatrix: tile t, 8-row half sel
     uint32_t rk[4], rv[4];
     int keyk[4], keyv[4];
@@ -354,8 +371,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         const int tv = FP8 ? tk : 16 * t + lrow + (lmat >> 1) * 8;          // V rows (bf16 PV)
         rk[t] = row_of(tk) + k_half;
         rv[t] = row_of(tv) + v_half;
-        keyk[t] = (tk * C::NX) & 7;
-        keyv[t] = (tv * C::NX) & 7;
+        keyk[t] = key_of(tk, 0);  // the key of half x is key_of(t, x): + x when token-major
+        keyv[t] = key_of(tv, 0);
     }
 
     SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
@@ -449,8 +466,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                 auto zero_v = [&](int a0, int a1) {
                     for (int e = lane; e < (a1 - a0) * C::NX * 8; e += 32) {
                         const int tok = a0 + e / (C::NX * 8), c16 = e % (C::NX * 8);
-                        uint4 *vr = reinterpret_cast<uint4 *>(stage_ptr + row_of(tok) + v_half);
-                        vr[c16] = make_uint4(0u, 0u, 0u, 0u);
+                        uint4 *vr = reinterpret_cast<uint4 *>(stage_ptr + row_of(tok) + v_half + (c16 >> 3) * xstride);
+                        vr[c16 & 7] = make_uint4(0u, 0u, 0u, 0u);
                     }
                 };
                 if (nskip > 0) zero_v(0, nskip);     // nskip <= nvalid: the ranges do not overlap
@@ -470,7 +487,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                     for (int t = 0; t < 4; ++t) {
                         const int d = ks * 16 + (lmat >> 1) * 8;
                         const int x = d >> 6;
-                        const uint32_t addr = s_base + rk[t] + x * 128 + ((((d & 63) >> 3) ^ (keyk[t] + x)) << 4);
+                        const uint32_t addr =
+                            s_base + rk[t] + x * xstride + ((((d & 63) >> 3) ^ (keyk[t] + (HM ? 0 : x))) << 4);
                         uint32_t a[4];
                         ldsm_x4(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
@@ -563,7 +581,8 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                     for (int t = 0; t < 4; ++t) {
                         const int d = mt * 16 + (lmat & 1) * 8;
                         const int x = d >> 6;
-                        const uint32_t addr = s_base + rv[t] + x * 128 + ((((d & 63) >> 3) ^ (keyv[t] + x)) << 4);
+                        const uint32_t addr =
+                            s_base + rv[t] + x * xstride + ((((d & 63) >> 3) ^ (keyv[t] + (HM ? 0 : x))) << 4);
                         uint32_t a[4];
                         ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll

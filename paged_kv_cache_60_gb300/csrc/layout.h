@@ -97,6 +97,7 @@ struct GqaParams {
     int32_t window;                // sliding window in tokens (0: none)
     const float *sinks;            // [H_q] attention-sink logits (natural-log units) or null
     int32_t cluster_merge;         // 1: fixed split count 2..8, the splits merge inside a cluster (no combine)
+    int32_t half_major;            // 1: the tensor maps deliver boxes as [pool][half][token][128 B]
     int32_t log2_box_tokens;       // box_tokens is 8, 16, 32 or 64
     int32_t kv_swap;               // 1: the V pool lies below the K pool (its rows come first in a box)
     int32_t kv_combined;           // 1: one 5-D map covers both pools; 0: one 4-D map per pool
