@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ GqaParams p) {
     using C = GqaCfg<D, FP8, NQ, WPC>;
+    // 256-byte rows land half-major in the builds with a window or several
+    // query tokens (the host builds the tensor maps to match: p.half_major)
+    constexpr bool HM = WIN && C::NX > 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *sm_u = reinterpret_cast<float *>(smem + C::OFF_U);
@@ -309,12 +312,12 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                         const int in_page = (P > kChunk) ? (tok % P) : 0;
                         uint8_t *st = smem + (size_t)stage * C::STAGE + lane * box_bytes;
                         if (p.kv_combined) {
-                            if (p.half_major)
+                            if constexpr (HM)
                                 tma_load_5d(st, &tm_kv, &full[stage], 0, pg * P + in_page, 0, h, 0, pol);
                             else
                                 tma_load_5d(st, &tm_kv, &full[stage], 0, 0, h, pg * P + in_page, 0, pol);
                         } else {  // K map in tm_kv, V map in tm_v, same box image
-                            if (p.half_major) {
+                            if constexpr (HM) {
                                 tma_load_4d(st, &tm_kv, &full[stage], 0, pg * P + in_page, 0, h, pol);
                                 tma_load_4d(st + box_bytes / 2, &tm_v, &full[stage], 0, pg * P + in_page, 0, h, pol);
                             } else {
@@ -352,7 +355,6 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
     // [half][token][128 B], in the builds with several query tokens or a
     // window, which do more arithmetic per byte: key t & 7, no conflict.
     // With NX = 1 the two are the same.
-    constexpr bool HM = WIN && C::NX > 1;
     const int bt = p.box_tokens, lbt = p.log2_box_tokens;
     const uint32_t half_bytes = (uint32_t)bt * C::NX * 128u;   // one pool's part of a box
     const uint32_t xstride = HM ? (uint32_t)bt * 128u : 128u;  // half 0 -> half 1 of a row
