@@ -69,8 +69,8 @@ struct GqaCfg {
     // With several query tokens (NQ > 1) a warp holds NQ times the state and
     // the kernel runs one CTA per SM: 6 or 7 consumer warps keep at most two
     // warps on each SM sub-partition, so a thread may use up to 255 registers.
-    static constexpr int NCW =
-        WPC > 1 ? 6 : (NQ > 1 ? (D == 128 && !FP8 ? 6 : 7) : (FP8 ? 10 : (D == 64 ? 5 : 6)));
+    static constexpr int NCW = WPC == 4 ? 8
+                               : WPC > 1 ? 6 : (NQ > 1 ? (D == 128 && !FP8 ? 6 : 7) : (FP8 ? 10 : (D == 64 ? 5 : 6)));
     static constexpr int NG = NCW / WPC;
     static constexpr int NS = NCW == 5 ? 5 : NCW;
     static_assert(NCW % WPC == 0 && NS % NG == 0, "stage ownership must be fixed per warp group");
@@ -750,7 +750,8 @@ static cudaError_t launch_one(const CUtensorMap &tkv, const CUtensorMap &tv, con
 cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMap &tv, const GqaParams &p,
                        cudaStream_t stream, bool pdl) {
     // one token without a window: the lean build; every other shape carries the
-    // window logic. Three or four query tokens: a pair of warps per chunk, two each.
+    // window logic. Three or four query tokens: four warps per chunk, one token
+    // each, at D = 64 (8 consumer warps); a pair of warps, two each, at D = 128.
     if (p.s_q == 1 && p.window == 0) {
         if (!fp8 && D == 64) return launch_one<64, false, 1, 1, false>(tkv, tv, p, stream, pdl);
         if (!fp8 && D == 128) return launch_one<128, false, 1, 1, false>(tkv, tv, p, stream, pdl);
@@ -764,7 +765,7 @@ cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMa
         if (!fp8 && D == 128) return launch_one<128, false, 2, 1, true>(tkv, tv, p, stream, pdl);
         if (fp8 && D == 128) return launch_one<128, true, 2, 1, true>(tkv, tv, p, stream, pdl);
     } else if (p.s_q <= 4) {
-        if (!fp8 && D == 64) return launch_one<64, false, 2, 2, true>(tkv, tv, p, stream, pdl);
+        if (!fp8 && D == 64) return launch_one<64, false, 1, 4, true>(tkv, tv, p, stream, pdl);
         if (!fp8 && D == 128) return launch_one<128, false, 2, 2, true>(tkv, tv, p, stream, pdl);
         if (fp8 && D == 128) return launch_one<128, true, 2, 2, true>(tkv, tv, p, stream, pdl);
     }
