@@ -303,11 +303,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, const uint4 &v) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
 // earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
@@ -338,14 +333,6 @@ __device__ __forceinline__ bool mbar_wait_warp_cluster(uint64_t *bar, uint32_t p
             if (__shfl_sync(0xffffffffu, stop, 0)) return false;
         }
     }
-}
-// 16-byte store into another CTA's shared memory that counts its bytes on
-// that CTA's mbarrier (complete_tx) instead of ordering through a fence.
-__device__ __forceinline__ void st_async_v4(uint32_t caddr, const uint4 &v, uint32_t cbar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     caddr),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cbar)
-                 : "memory");
 }
 // Arrive on another CTA's mbarrier without ordering earlier memory accesses
 // (for acknowledgements whose loads have already been consumed).

@@ -84,7 +84,7 @@ struct GqaCfg {
     static constexpr int OFF_W = OFF_L + NCW * G * 4;
     static constexpr int OFF_FIN = OFF_W + NCW * G * 4;
     static constexpr int OFF_BAR = (OFF_FIN + 4 * G * 4 + 7) / 8 * 8;
-    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8 + 16;  // + the cluster merge's two barriers
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * NS * 8;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + alignment slack
     static constexpr int MIN_BLOCKS = (D == 64 && !FP8 && NQ == 1 && WPC == 1) ? 2 : 1;
     static_assert(ROW % 128 == 0, "rows must be whole 128-byte boxes");
@@ -93,39 +93,42 @@ struct GqaCfg {
 
 // Split merge inside a cluster (fixed split count S <= 8): the S CTAs of a
 // (request, KV head) form one thread-block cluster; each has left its split's
-// normalised partial (o, lse) for every row in its own shared memory. Once
-// all S have signalled, CTA rank r merges dims [floor(r D / S),
-// floor((r + 1) D / S)) of every row by the rule of the combine kernel
-// (lse = M + ln sum e^(lse_s - M), out = sum e^(lse_s - lse) o_s, splits in
-// index order), adds the attention
-// sink and writes out and lse. It then waits until every split has finished
-// reading its memory before it exits. Called by the consumer warps only.
+// normalised partial (o, lse) for every row in its own shared memory. After
+// a cluster barrier (arrive releases this CTA's partial, wait acquires the
+// others'; a CTA's threads reaching it have also started, so no earlier
+// barrier is needed before reading another CTA's memory), CTA rank r merges
+// dims [floor(r D / S), floor((r + 1) D / S)) of every row from distributed
+// shared memory by the rule of the combine kernel (lse = M + ln sum
+// e^(lse_s - M), out = sum e^(lse_s - lse) o_s, splits in index order), adds
+// the attention sink and writes out and lse. A second cluster barrier keeps
+// every CTA resident until all have finished reading its memory. Called by
+// the consumer warps only; the producer warp has exited by then (the barrier
+// does not wait for exited threads).
+struct MergeArgs {
+    void *out;
+    float *lse;
+    const float *sinks;
+    int s_q, H_q, S;
+};
+
+// Out of line (its registers stay out of the main loop's allocation); the
+// kernel parameters it needs come by value.
 template <int D>
-__device__ __forceinline__ void cluster_merge(const GqaParams &p, float *xo, float *xl, uint64_t *xready,
-                                              uint64_t *xdone, const volatile int *never, int b, int h,
-                                              bool aborted) {
+__device__ __noinline__ void cluster_merge(const MergeArgs p, float *xo, float *xl, int b, int h, bool aborted) {
     constexpr int G = 8;
     constexpr float kLog2e = 1.4426950408889634f;
     const int nthr = blockDim.x - 32;  // consumer threads
     const int ctid = threadIdx.x;
-    const int S = p.splits;
+    const int S = p.S;
     const int rows_cta = p.s_q * G;
     if (aborted || b < 0) {
         // no valid partial: weight 0 for every row
         for (int r = ctid; r < rows_cta; r += nthr) xl[r] = -INFINITY;
     }
-    named_barrier_sync(1, nthr);
-    cluster_wait_all();  // the other splits' barriers are initialised (their threads arrived at start)
-    if (ctid == 0) {
-        fence_acq_rel_cluster();  // this CTA's partial, before the arrivals below release it
-        for (int q = 0; q < S; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(xready), (uint32_t)q));
-    }
-    const int lane = ctid & 31;
-    bool ok = mbar_wait_warp_cluster(xready, 0, never, p.wait_limit_ns);
-    ok = !named_barrier_or(1, nthr, !ok);  // every consumer warp saw all S arrivals
-    if (!ok) {
-        if (ctid == 0) atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
-    } else if (b >= 0) {
+    __syncwarp();          // the cluster barrier instructions below are warp-aligned
+    cluster_arrive_all();  // this thread's share of the partial is written (release)
+    cluster_wait_all();    // every split's partial is visible (acquire)
+    if (b >= 0) {
         const uint32_t rank = cluster_ctarank();
         const int d0 = (int)rank * D / S, dpc = ((int)rank + 1) * D / S - d0;  // this CTA's dims
         const uint32_t xo_s = smem_u32(xo), xl_s = smem_u32(xl);
@@ -165,12 +168,11 @@ __device__ __forceinline__ void cluster_merge(const GqaParams &p, float *xo, flo
             if (rank == 0 && idx % dpc == 0) p.lse[orow] = lse_v;
         }
     }
-    // this CTA's loads from the others are done: tell them, then wait until they are done with ours
-    named_barrier_sync(1, nthr);
-    if (ctid == 0)
-        for (int q = 0; q < S; ++q) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(xdone), (uint32_t)q));
-    if (!mbar_wait_warp_cluster(xdone, 0, never, p.wait_limit_ns) && lane == 0)
-        atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
+    // this thread's loads from the other splits are done; wait until every
+    // split is done with this one's memory before it exits
+    __syncwarp();
+    cluster_arrive_all();
+    cluster_wait_all();
 }
 
 // NQ x WPC: query tokens per request the kernel is compiled for (s_q <=
@@ -195,10 +197,6 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *empty = full + C::NS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
-    // cluster merge: partials of every split ready / read by every split; waits
-    // on them ignore the abort flag (a word that stays 0)
-    uint64_t *xready = empty + C::NS, *xdone = xready + 1;
-    const volatile int *never = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int part = blockIdx.x, h = blockIdx.y;
@@ -209,11 +207,6 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
             mbar_init(&empty[i], WPC);  // every warp of the chunk's group
         }
         *abort_flag = 0;
-        abort_flag[1] = 0;
-        if (p.cluster_merge) {
-            mbar_init(xready, p.splits);  // one arrival from each split of the request
-            mbar_init(xdone, p.splits);
-        }
 #ifdef DA_PAGE_TRACE
         mbar_init(reinterpret_cast<uint64_t *>(smem + C::OFF_FLAG + 8), 1);  // never arrived at
 #endif
@@ -225,9 +218,6 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         if (!p.kv_combined) prefetch_tmap(&tm_v);
     }
     __syncthreads();
-    // every split's merge barriers exist before any remote arrival: arrive here,
-    // wait (consumer threads) just before the merge's first remote arrival
-    if (p.cluster_merge) cluster_arrive_all();
     pdl_wait();
     pdl_launch_dependents();
 
@@ -260,7 +250,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         if (lane >= nb) return;
         const uint64_t pol = policy_evict_first();
         const uint32_t box_bytes = 2u * bt * C::NX * 128u;
-        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
+        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len, p.s_q, WIN ? p.window : 0, 0);
         int i = 0;
         bool aborted = false;
         Seg sg;
@@ -377,7 +367,7 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         keyv[t] = key_of(tv, 0);
     }
 
-    SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
+    SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len, p.s_q, WIN ? p.window : 0, 0);
     int i = 0;
     Seg sg;
     int merge_b = -1;  // cluster merge: the request of this CTA's (single) segment
@@ -669,7 +659,6 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                         sm_w[w * C::G + g] = wt;
                         Ls += wt * sm_l[w * C::G + g];
                     }
-                    sm_fin[g] = Ls;
                     // lse over the tokens; a request with a single split gets its
                     // attention sink here (the combine adds it to the others)
                     float lse_v = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -INFINITY, fac = 1.f;
@@ -678,26 +667,34 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                         fac = (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
                         lse_v = tot;
                     }
-                    sm_fin[C::G + g] = fac;
+                    sm_fin[g] = (Ls > 0.f) ? vscale * fac / Ls : 0.f;  // out = u * this
                     sm_fin[2 * C::G + g] = lse_v;
                 }
                 named_barrier_sync(1, C::NCW * 32);
                 const size_t row0 = (size_t)jj * p.H_q + (size_t)h * C::G;  // row of head g = row0 + g
-                for (int idx = ctid; idx < C::G * D; idx += C::NCW * 32) {
-                    const int g = idx / D, d = idx % D;
-                    float u = 0.f;
+                // four consecutive dims per thread and step
+                for (int idx = ctid; idx < C::G * (D / 4); idx += C::NCW * 32) {
+                    const int g = idx / (D / 4), d = (idx % (D / 4)) * 4;
+                    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int w = ow; w < C::NCW; w += WPC)
-                        u += sm_w[w * C::G + g] * sm_u[((size_t)w * C::G + g) * C::UPAD + d];
-                    const float Ls = sm_fin[g];
-                    const float o = (Ls > 0.f) ? (u / Ls) * vscale * sm_fin[C::G + g] : 0.f;
+                    for (int w = ow; w < C::NCW; w += WPC) {
+                        const float wt = sm_w[w * C::G + g];
+                        const float4 v = *reinterpret_cast<const float4 *>(sm_u + ((size_t)w * C::G + g) * C::UPAD + d);
+                        u.x += wt * v.x;
+                        u.y += wt * v.y;
+                        u.z += wt * v.z;
+                        u.w += wt * v.w;
+                    }
+                    const float f = sm_fin[g];
+                    const float4 o = make_float4(u.x * f, u.y * f, u.z * f, u.w * f);
                     if (direct)
-                        reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)sb * rows + row0 + g) * D + d] =
-                            __float2bfloat16_rn(o);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                                   ((size_t)sb * rows + row0 + g) * D + d) =
+                            make_uint2(pack_bf16(o.x, o.y), pack_bf16(o.z, o.w));
                     else if (p.cluster_merge)
-                        xo[(size_t)(jj * C::G + g) * D + d] = o;
+                        *reinterpret_cast<float4 *>(xo + (size_t)(jj * C::G + g) * D + d) = o;
                     else if (split_ok)
-                        p.meta.o_part[((size_t)split * rows + row0 + g) * D + d] = o;
+                        *reinterpret_cast<float4 *>(p.meta.o_part + ((size_t)split * rows + row0 + g) * D + d) = o;
                 }
                 if (ctid < C::G) {
                     const int g = ctid;
@@ -713,7 +710,9 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
         }
         if (named_barrier_or(1, C::NCW * 32, *abort_flag != 0)) break;
     }
-    if (p.cluster_merge) cluster_merge<D>(p, xo, xl, xready, xdone, never, merge_b, h, *abort_flag != 0);
+    if (p.cluster_merge)
+        cluster_merge<D>(MergeArgs{p.out, p.lse, p.sinks, p.s_q, p.H_q, p.splits}, xo, xl, merge_b, h,
+                         *abort_flag != 0);
 }
 
 template <int D, bool FP8, int NQ, int WPC, bool WIN>

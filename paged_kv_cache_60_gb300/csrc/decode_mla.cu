@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, 256, 0, 1);
             const int ks0 = 2 * (int)rank;  // first 16-dim step of this CTA's 288 contraction dims in its window
-            SegWalker wq = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
+            SegWalker wq = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len, 1, 0, p.topk);
             SegWalker wp = wq;
             auto next_seg = [](SegWalker &w, int &n) -> bool {
                 Seg g;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         // RoPE values (g >= 16, 32 bytes each). All loads of a chunk are in
         // flight while the warp waits for its tile of the ring.
         const int dt = threadIdx.x - 5 * 32;  // 0 .. 255
-        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
+        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len, 1, 0, p.topk);
         Seg sg;
         int ic = 0;
         bool ok = true;
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         const uint32_t xfull_peer = mapa_shared(smem_u32(xfull), peer);
         const uint32_t xfree_peer = mapa_shared(smem_u32(xfree), peer);
         const int d_base = 256 * (int)rank;        // value dims held by this CTA: [d_base, d_base + 256)
-        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len);
+        SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len, 1, 0, p.topk);
         Seg sg;
         int ic = 0, seg = 0;
         bool ok = true;

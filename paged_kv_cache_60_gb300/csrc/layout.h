@@ -83,6 +83,13 @@ __host__ __device__ inline int window_start(int L, int s_q, int window) {
     return (window > 0 && st > 0) ? st : 0;
 }
 
+// Chunks of a request of (clamped) length L in the schedule: the listed
+// positions for sparse decode, else the chunks from the one holding the
+// window's first token to the end.
+__host__ __device__ inline int chunks_of(int L, int s_q, int window, int topk) {
+    return topk > 0 ? (topk + kChunk - 1) / kChunk : (L + kChunk - 1) / kChunk - window_start(L, s_q, window) / kChunk;
+}
+
 struct GqaParams {
     const void *q;                 // bf16 [B][s_q][H_q][D]
     const int32_t *block_table;    // [B][max_pages]

@@ -82,8 +82,7 @@ __global__ void __launch_bounds__(1024) sched_meta_kernel(const __grid_constant_
                 L = p.max_len;
             }
             // sparse decode: the request's topk listed positions, whatever its length
-            n = p.topk > 0 ? (p.topk + kChunk - 1) / kChunk
-                           : (L + kChunk - 1) / kChunk - window_start(L, p.s_q, p.window) / kChunk;
+            n = chunks_of(L, p.s_q, p.window, p.topk);
         }
         int tile_total;
         const int incl = block_incl_scan(n, warp_sums, tile_total);

@@ -13,10 +13,12 @@ struct Seg {
 };
 
 // Walks the segments of one part. The first segment comes entirely from the
-// part record (no dependent loads); later ones read the per-request arrays.
+// part record, with no dependent load: its request's chunk count follows from
+// the record's length as the scheduling kernel computed it (chunk_offset[b + 1]
+// - chunk_offset[b] = chunks_of(L)); later segments read the per-request arrays.
 struct SegWalker {
     const int32_t *chunk_offset, *split_offset, *num_splits, *seqlens;
-    int B, max_len, b, s, c, c1;
+    int B, max_len, b, s, c, c1, s_q, window, topk;
     int co0, L0, so0, ns0;
     bool first, pending_empty;
     __device__ bool next(Seg &g) {
@@ -35,7 +37,7 @@ struct SegWalker {
         int cb, ce;
         if (first) {
             cb = co0;
-            ce = chunk_offset[b + 1];
+            ce = co0 + chunks_of(L0, s_q, window, topk);
             if (ce <= c) return false;  // inconsistent record
         } else {
             while (b < B && chunk_offset[b + 1] <= c) {
@@ -69,7 +71,8 @@ struct SegWalker {
 };
 
 __device__ __forceinline__ SegWalker make_walker(const MetaView &mv, const int4 r0, const int4 r1, int B,
-                                                 const int32_t *seqlens, int max_len) {
+                                                 const int32_t *seqlens, int max_len, int s_q, int window,
+                                                 int topk) {
     SegWalker w;
     w.chunk_offset = mv.chunk_offset;
     w.split_offset = mv.split_offset;
@@ -77,6 +80,9 @@ __device__ __forceinline__ SegWalker make_walker(const MetaView &mv, const int4 
     w.seqlens = seqlens;
     w.B = B;
     w.max_len = max_len;
+    w.s_q = s_q;
+    w.window = window;
+    w.topk = topk;
     const bool valid = r0.x >= 0 && r0.x < B && r0.z <= r0.w;
     w.b = valid ? r0.x : -1;
     w.s = r0.y;
