@@ -173,15 +173,6 @@ __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *m, uin
         "l"(policy)
         : "memory");
 }
-// Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                          uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
 
 // ------------------------------------------------------------------ warp MMA
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -378,15 +369,8 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, i
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-// Same, with the A operand read from tensor memory (rows in lanes, K packed
-// two bf16 per 32-bit column).
+// tcgen05.mma kind::f16 with the A operand read from tensor memory (rows in lanes,
+// K packed two bf16 per 32-bit column) and B from a shared-memory descriptor.
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                  bool accumulate) {
     asm volatile(
