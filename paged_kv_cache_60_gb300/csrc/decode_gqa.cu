@@ -121,19 +121,24 @@ __device__ __noinline__ void cluster_merge(const MergeArgs p, float *xo, float *
     const int ctid = threadIdx.x;
     const int S = p.S;
     const int rows_cta = p.s_q * G;
+    const uint32_t rank = cluster_ctarank();
+    const int d0 = (int)rank * D / S, dpc = ((int)rank + 1) * D / S - d0;  // this CTA's dims
+    // whole warps the merge needs; the others leave now (their writes are
+    // ordered before the remaining threads' release by the CTA barrier that
+    // ended the segment, and exited threads do not hold up the cluster barrier)
+    const int keep = min(nthr, (rows_cta * dpc + 31) / 32 * 32);
     if (aborted || b < 0) {
         // no valid partial: weight 0 for every row
         for (int r = ctid; r < rows_cta; r += nthr) xl[r] = -INFINITY;
     }
+    if (ctid >= keep) return;
     __syncwarp();          // the cluster barrier instructions below are warp-aligned
     cluster_arrive_all();  // this thread's share of the partial is written (release)
     cluster_wait_all();    // every split's partial is visible (acquire)
     if (b >= 0) {
-        const uint32_t rank = cluster_ctarank();
-        const int d0 = (int)rank * D / S, dpc = ((int)rank + 1) * D / S - d0;  // this CTA's dims
         const uint32_t xo_s = smem_u32(xo), xl_s = smem_u32(xl);
         const size_t rows = (size_t)p.s_q * p.H_q;
-        for (int idx = ctid; idx < rows_cta * dpc; idx += nthr) {
+        for (int idx = ctid; idx < rows_cta * dpc; idx += keep) {
             const int r = idx / dpc, d = d0 + idx % dpc;
             // every split's lse and value in one round of loads
             float ls[8], ov[8];
