@@ -58,7 +58,11 @@ typedef enum {
     /* k_pool: 656-byte tokens [num_pages][page_size][1][656] (FlashMLA page,
      * section "数据加载"): 512 e4m3, 4 fp32 scales (one per 128 values), 64 bf16
      * RoPE values. K = the 576 dequantised values, V = the first 512. v_pool
-     * must be NULL or equal to k_pool; H_kv = 1, D_qk = 576, D_v = 512. */
+     * must be NULL or equal to k_pool; H_kv = 1, D_qk = 576, D_v = 512.
+     * Input contract: the e4m3 bytes of a token the call reads hold finite
+     * codes (what the quantiser, decode_attn_append_kv, writes: it saturates
+     * at +-448 and never emits 0x7F / 0xFF). The decoder widens codes by bit
+     * moves, which read 0x7F / 0xFF as +-480 rather than NaN. */
     DA_KV_FP8_MLA656 = 2
 } da_kv_dtype;
 
@@ -100,6 +104,9 @@ typedef struct {
 #define DA_DEV_META_MISMATCH  16   /* sched_meta was built for another desc */
 
 /*
+ * Library plumbing from here to decode_attn_num_parts: no page defines these
+ * calls; they size and describe the caller-owned sched_meta buffer.
+ *
  * Size in bytes of the sched_meta buffer for this desc (host only, no CUDA
  * call except an SM-count query when desc->num_sms is 0). The buffer holds the
  * scheduling metadata, the split-KV partials (fp32 o and lse per split and
@@ -258,7 +265,7 @@ int decode_attn_append_kv(const da_desc *desc, const void *k_new, const void *v_
 
 /*
  * Reads the device error word of sched_meta into *device_error (host int32).
- * Synchronises `stream`.
+ * Synchronises `stream`. Library plumbing: no page defines this call.
  */
 int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStream_t stream);
 
@@ -278,11 +285,18 @@ int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStr
  * array of DA_STATIC_SCRATCH_BYTES that the library owns; every GPU that loads
  * the library keeps it until the process exits. Problems whose
  * decode_attn_sched_meta_bytes exceeds that size are rejected with
- * DA_ERR_META_SIZE. The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress, with that device current): make that first
- * call before any stream capture. Every call reuses the same array and leaves
- * its contents behind; the scheduling kernel rewrites all it reads, so nothing
- * needs clearing, but calls whose work overlaps on the GPU race on the array.
+ * DA_ERR_META_SIZE. With the 656-byte format the automatic split count
+ * (desc->splits = 0) of a GB300 needs about 20 MB and is rejected: pass a fixed
+ * split count or a smaller desc->num_sms. Sparse decode (desc->topk > 0) needs
+ * indices, which this call cannot take: DA_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current): make that first call
+ * before any stream capture. The address is kept per device and CUDA context;
+ * after a device reset the next call looks it up again. Every call reuses the
+ * same array and leaves its contents behind; the scheduling kernel rewrites
+ * all it reads, so nothing needs clearing, but calls whose work overlaps on
+ * the GPU race on the array. Every argument is checked on the host before
+ * anything is launched, so a rejected call leaves the array untouched.
  * Arguments, layouts and errors are those of decode_attn_fwd; device errors
  * land in the array's error word and are not readable from outside.
  */
@@ -290,7 +304,8 @@ int decode_attn_fwd_static_scratch(const da_desc *desc, const void *q, const voi
                                    const float *k_scale, const float *v_scale, const int32_t *block_table,
                                    const int32_t *cache_seqlens, void *out, float *lse, cudaStream_t stream);
 
-/* Static description of a return code (never NULL). */
+/* Static description of a return code (never NULL). Library plumbing: no
+ * page defines this call. */
 const char *decode_attn_strerror(int code);
 
 #ifdef DA_PAGE_TRACE

@@ -23,6 +23,15 @@ KV_FP8 = 1
 KV_MLA656 = 2
 
 DA_OK = 0
+DA_ERR_NULL = -1
+DA_ERR_DIMS = -2
+DA_ERR_UNSUPPORTED = -3
+DA_ERR_ALIGN = -4
+DA_ERR_SPLITS = -5
+DA_ERR_META_SIZE = -6
+DA_ERR_CUDA = -7
+DA_ERR_SCALE = -8
+
 DA_DEV_BAD_PAGE = 1
 DA_DEV_SEQ_TOO_LONG = 2
 DA_DEV_NEG_LEN = 4

@@ -20,6 +20,9 @@ cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stre
 int mla_ctas_per_part();
 bool mla_kernel_available();
 int mla_max_parts();
+int check_fwd_args(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                   const float *k_scale, const float *v_scale, const int32_t *block_table,
+                   const int32_t *cache_seqlens, const void *out, const float *lse, const da_launch_opts *opts);
 }  // namespace da
 
 using namespace da;
@@ -221,6 +224,37 @@ int make_kv_map(CUtensorMap *m, const void *base, uint64_t pool_dist, bool two_p
 
 }  // namespace
 
+// Every host-side check of decode_attn_fwd_ex that does not involve the
+// sched_meta buffer (desc, pointers, alignment, scales, optional inputs);
+// returns DA_OK or the first error. No CUDA call beyond an SM-count query.
+int da::check_fwd_args(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
+                       const float *k_scale, const float *v_scale, const int32_t *block_table,
+                       const int32_t *cache_seqlens, const void *out, const float *lse,
+                       const da_launch_opts *opts) {
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    const bool mla = is_mla(desc);
+    if (!q || !k_pool || !block_table || !cache_seqlens || !out || !lse) return DA_ERR_NULL;
+    if (!mla && !v_pool) return DA_ERR_NULL;
+    if (mla && v_pool && v_pool != k_pool) return DA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool)) || !aligned16(block_table) ||
+        !aligned16(cache_seqlens) || !aligned16(out) || !aligned16(lse))
+        return DA_ERR_ALIGN;
+    if (desc->kv_dtype == DA_KV_FP8_PER_TENSOR) {
+        if (!k_scale || !v_scale) return DA_ERR_SCALE;
+        if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+            return DA_ERR_ALIGN;
+    }
+    const float *sinks = opts ? opts->sinks : nullptr;
+    if (sinks && mla) return DA_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(sinks) & 3u) return DA_ERR_ALIGN;
+    const int32_t *indices = opts ? opts->indices : nullptr;
+    if (desc->topk > 0 && !indices) return DA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(indices) & 3u) return DA_ERR_ALIGN;
+    if (!mla && (int64_t)desc->page_size * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+    return DA_OK;
+}
+
 extern "C" {
 
 int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes) {
@@ -299,24 +333,14 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
     int rc = make_layout(desc, &L);
     if (rc) return rc;
     const bool mla = is_mla(desc);
-    if (!q || !k_pool || !block_table || !cache_seqlens || !sched_meta || !out || !lse) return DA_ERR_NULL;
-    if (!mla && !v_pool) return DA_ERR_NULL;
-    if (mla && v_pool && v_pool != k_pool) return DA_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_pool) || (v_pool && !aligned16(v_pool)) || !aligned16(block_table) ||
-        !aligned16(cache_seqlens) || !aligned16(sched_meta) || !aligned16(out) || !aligned16(lse))
-        return DA_ERR_ALIGN;
-    if (desc->kv_dtype == DA_KV_FP8_PER_TENSOR) {
-        if (!k_scale || !v_scale) return DA_ERR_SCALE;
-        if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
-            return DA_ERR_ALIGN;
-    }
+    if ((rc = check_fwd_args(desc, q, k_pool, v_pool, k_scale, v_scale, block_table, cache_seqlens, out, lse,
+                             opts)))
+        return rc;
+    if (!sched_meta) return DA_ERR_NULL;
+    if (!aligned16(sched_meta)) return DA_ERR_ALIGN;
     if (sched_meta_bytes < L.total) return DA_ERR_META_SIZE;
     const float *sinks = opts ? opts->sinks : nullptr;
-    if (sinks && mla) return DA_ERR_UNSUPPORTED;
-    if (reinterpret_cast<uintptr_t>(sinks) & 3u) return DA_ERR_ALIGN;
     const int32_t *indices = opts ? opts->indices : nullptr;
-    if (desc->topk > 0 && !indices) return DA_ERR_NULL;
-    if (reinterpret_cast<uintptr_t>(indices) & 3u) return DA_ERR_ALIGN;
     const bool pdl = opts ? opts->use_pdl != 0 : true;
     const float sigma = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->D_qk);
     const MetaView mv = meta_view(sched_meta, L);
@@ -328,7 +352,6 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         const int es = fp8 ? 1 : 2;
         const int P = desc->page_size;
         const int box_tok = P < kChunk ? P : kChunk;
-        if ((int64_t)P * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
         // one map over both pools when their distance can be a tensor-map
         // stride (a multiple of 16 below 2^40, not overlapping); else one per pool
         const uint64_t pool_bytes = (uint64_t)desc->num_pages * P * desc->H_kv * desc->D_qk * es;

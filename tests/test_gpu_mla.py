@@ -102,9 +102,9 @@ def test_mla_bad_page_sets_error_word():
     assert da.get_error(meta) & da.DA_DEV_BAD_PAGE
 
 
-def test_mla_workload_sampled_parity():
+def test_mla_workload_parity():
     """The 32-request latent-token workload (lengths log-uniform in [4096, 131072]),
-    full launch; the oracle checks the longest, the shortest and one more request."""
+    full launch; every request against the oracle."""
     w = make_workload(spec_by_name("mla_fp8"))
     out, lse, meta, desc = run(w)
     torch.cuda.synchronize()
@@ -112,9 +112,8 @@ def test_mla_workload_sampled_parity():
     got = read_meta(meta, desc)
     ref = sched_ref(w.lengths, 1, 0, _auto_sms(desc), cpc=2)
     assert got["parts"] == ref.parts and got["split_offset"] == ref.split_offset
-    order = sorted(range(w.spec.B), key=lambda b: -w.lengths[b])
-    heads = sorted({(order[0], 0), (order[-1], 0), (order[len(order) // 2], 0)})
-    ref_out, ref_lse = oracle.attend(w, heads=heads)
+    ref_out, ref_lse = oracle.attend(w)
+    assert not torch.isnan(ref_lse).any()
     e_out, e_lse = max_err(out, lse, ref_out, ref_lse)
     assert e_out <= OUT_TOL, e_out
     assert e_lse <= LSE_TOL, e_lse

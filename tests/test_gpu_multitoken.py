@@ -89,18 +89,15 @@ def test_last_draft_matches_single_token_kernel():
 
 
 @pytest.mark.parametrize("name", ["spec2_gqa_bf16", "spec4_gqa_d64", "spec2_fp8_gqa", "spec4_gqa_bf16"])
-def test_multitoken_bench_workloads_sampled(name):
+def test_multitoken_bench_workloads(name):
     """The benchmark's multi-token workloads at full size, in its launch
-    configuration; the oracle checks a sample of (request, KV head) units."""
+    configuration; every (request, KV head) unit against the oracle."""
     spec = spec_by_name(name)
     w = make_workload(spec)
     out, lse, _, _ = run(w)
     torch.cuda.synchronize()
-    g = torch.Generator().manual_seed(1)
-    n = 6 if spec.kv_dtype == KV_FP8 else 12
-    picks = torch.randperm(spec.B * spec.H_kv, generator=g)[:n].tolist()
-    heads = [(p // spec.H_kv, p % spec.H_kv) for p in picks]
-    ref_out, ref_lse = oracle.attend_multi(w, heads=heads)
+    ref_out, ref_lse = oracle.attend_multi(w)
+    assert not torch.isnan(ref_lse).any()
     e_out, e_lse = max_err(out.view(ref_out.shape), lse.view(ref_lse.shape), ref_out, ref_lse)
     assert e_out <= OUT_TOL and e_lse <= LSE_TOL, (e_out, e_lse)
 

@@ -222,19 +222,11 @@ def test_too_long_sequence_is_clamped_and_flagged():
 
 # ------------------------------------------------------------------ the five workloads
 
-def _sample_heads(w, n, seed):
-    rnd = random.Random(seed)
-    s = w.spec
-    order = sorted(range(s.B), key=lambda b: -w.lengths[b])
-    heads = {(order[0], 0), (order[-1], s.H_kv - 1)}
-    while len(heads) < min(n, s.B * s.H_kv):
-        heads.add((rnd.randrange(s.B), rnd.randrange(s.H_kv)))
-    return sorted(heads)
-
-
-@pytest.mark.parametrize("name,nsample", [("tiny_gqa_bf16", None), ("gqa_bf16_b8", None),
-                                          ("mixed_gqa_bf16", 10), ("fp8_gqa", 6)])
-def test_workload_parity(name, nsample):
+@pytest.mark.parametrize("name", ["tiny_gqa_bf16", "gqa_bf16_b8", "mixed_gqa_bf16", "fp8_gqa"])
+def test_workload_parity(name):
+    """The full-size workloads in the benchmark's launch configuration: every
+    output row against the oracle (the oracle computes every (request, KV
+    head) unit)."""
     w = make_workload(spec_by_name(name))
     out, lse, meta, desc = run(w)
     torch.cuda.synchronize()
@@ -242,8 +234,8 @@ def test_workload_parity(name, nsample):
     got = read_meta(meta, desc)
     ref = sched_ref(w.lengths, w.spec.H_kv, w.spec.splits, device_sms())
     assert got["parts"] == ref.parts and got["split_offset"] == ref.split_offset
-    heads = None if nsample is None else _sample_heads(w, nsample, 1)
-    ref_out, ref_lse = oracle.attend(w, heads=heads)
+    ref_out, ref_lse = oracle.attend(w)
+    assert not torch.isnan(ref_lse).any()
     e_out, e_lse = max_err(out, lse, ref_out, ref_lse)
     assert e_out <= OUT_TOL, (name, e_out)
     assert e_lse <= LSE_TOL, (name, e_lse)

@@ -106,16 +106,16 @@ def test_sinks_dominating_and_absent():
     assert (l_big - 60.0).abs().max().item() < 1e-5
 
 
-def test_window_sinks_bench_workload_sampled():
+def test_window_sinks_bench_workload():
+    """The window + sinks workload at full size: every (request, KV head) unit
+    against the oracle."""
     spec = spec_by_name("window_sinks_gqa_bf16")
     w = make_workload(spec)
     _drop_pages_before_window(w)
     out, lse, meta, _ = run(w)
     torch.cuda.synchronize()
     assert da.get_error(meta) == 0
-    g = torch.Generator().manual_seed(2)
-    picks = torch.randperm(spec.B * spec.H_kv, generator=g)[:16].tolist()
-    heads = [(p // spec.H_kv, p % spec.H_kv) for p in picks]
-    ref_out, ref_lse = oracle.attend_multi(w, heads=heads)
+    ref_out, ref_lse = oracle.attend_multi(w)
+    assert not torch.isnan(ref_lse).any()
     e_out, e_lse = max_err(out.view(ref_out.shape), lse.view(ref_lse.shape), ref_out, ref_lse)
     assert e_out <= OUT_TOL and e_lse <= LSE_TOL, (e_out, e_lse)
