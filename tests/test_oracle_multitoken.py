@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import WorkloadSpec, make_workload, KV_BF16, KV_FP8
+from workloads import WorkloadSpec, make_workload, KV_BF16, KV_FP8, KV_MLA656
 
 
 def _spec(**kw):
@@ -161,3 +161,66 @@ def test_windowed_split_and_combine_equals_unsplit(oracle_lib, splits):
     fin = ~torch.isneginf(lse[:, 0])
     assert torch.equal(torch.isneginf(l), ~fin)
     assert torch.allclose(l[fin], lse[:, 0][fin], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ the 656-byte latent token, two drafts
+
+def _mla_spec(**kw):
+    base = dict(name="m", B=4, H_kv=1, G=4, D_qk=576, D_v=512, page_size=16, kv_dtype=KV_MLA656,
+                lengths=[1, 2, 40, 0], splits=0, extra_pages=3, seed=9, s_q=2)
+    base.update(kw)
+    return WorkloadSpec(**base)
+
+
+def _mla_rows(w, b):
+    """K [L, 576] and V [L, 512] of request b in float64, decoded from the
+    656-byte rows with torch's float8_e4m3fn type, independently of the
+    oracle's decoder: 512 codes times their block's fp32 scale, rounded to
+    bf16 (the FlashMLA page's chain, section 计算环节一), then the 64 bf16 RoPE
+    values; V is the first 512."""
+    P = w.spec.page_size
+    ks = []
+    for t in range(w.lengths[b]):
+        row = w.k_pool[int(w.block_table[b, t // P]), t % P, 0]
+        codes = row[:512].view(torch.float8_e4m3fn).float()
+        scales = row[512:528].view(torch.float32).repeat_interleave(128)
+        nope = (codes * scales).to(torch.bfloat16).double()
+        rope = row[528:656].view(torch.bfloat16).double()
+        ks.append(torch.cat([nope, rope]))
+    if not ks:
+        return torch.zeros(0, 576, dtype=torch.float64), torch.zeros(0, 512, dtype=torch.float64)
+    K = torch.stack(ks)
+    return K, K[:, :512]
+
+
+def test_mla_two_drafts_masked_matrix(oracle_lib):
+    """Two query tokens on the latent format: per (request, query head) the
+    score matrix has one row per draft, later tokens set to -inf; torch's
+    softmax and logsumexp over K, V decoded independently give out and lse."""
+    spec = _mla_spec()
+    w = make_workload(spec, poison=False)
+    out, lse = oracle.attend_multi(w)
+    q = w.q.double().view(spec.B, 2, spec.H_q, 576)
+    for b, L in enumerate(w.lengths):
+        K, V = _mla_rows(w, b)
+        t = torch.arange(L).view(1, L)
+        pos = (L - 2 + torch.arange(2)).view(2, 1)
+        for hq in range(spec.H_q):
+            S = (w.softmax_scale * (q[b, :, hq] @ K.T)).masked_fill(~(t <= pos), float("-inf"))
+            for j in range(2):
+                if L - 1 + j <= 0:
+                    assert lse[b, j, hq] == float("-inf") and torch.all(out[b, j, hq] == 0)
+                    continue
+                assert abs(float(lse[b, j, hq] - torch.logsumexp(S[j], 0))) < 1e-11
+                ref_o = torch.softmax(S[j], 0) @ V
+                assert torch.allclose(out[b, j, hq], ref_o, rtol=0, atol=1e-11)
+
+
+def test_mla_last_draft_is_single_token_decode(oracle_lib):
+    spec = _mla_spec(lengths=[3, 70, 129, 1])
+    w = make_workload(spec, poison=False)
+    out, lse = oracle.attend_multi(w)
+    single = dataclasses.replace(w, spec=spec.with_(s_q=1), q=w.q[:, -1].contiguous())
+    ref_out, ref_lse = oracle.attend(single)
+    assert torch.equal(out[:, -1], ref_out)
+    assert torch.equal(lse[:, -1], ref_lse)
