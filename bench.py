@@ -512,9 +512,9 @@ def run_ours(args, rank, world, local):
     main_ms = value_us * 1e-3
     hbm_achieved = kv_bytes / (main_ms * 1e-3) / 1e9
     if key == "mla":
-        # tensor-bound: 2 (D_qk + D_v) flops per (token, query head); 424 flop per KV byte
+        # tensor-bound: 2 (D_qk + D_v) flops per (token, query head, query token); 424 flop per KV byte
         ntok = sum(min(L, spec.topk) for L in w.lengths) if spec.topk > 0 else sum(w.lengths)
-        flops = 2.0 * (spec.D_qk + spec.D_v) * spec.H_q * ntok
+        flops = 2.0 * (spec.D_qk + spec.D_v) * spec.H_q * spec.s_q * ntok
         achieved = flops / (main_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": round(achieved / tc_peak, 4), "traffic": traffic,

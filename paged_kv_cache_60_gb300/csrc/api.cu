@@ -17,9 +17,8 @@ cudaError_t launch_gqa(int D, bool fp8, const CUtensorMap &tkv, const CUtensorMa
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stream, bool pdl);
-int mla_ctas_per_part();
+int mla_ctas_per_part(int s_q);
 bool mla_kernel_available();
-int mla_max_parts();
 int check_fwd_args(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
                    const float *k_scale, const float *v_scale, const int32_t *block_table,
                    const int32_t *cache_seqlens, const void *out, const float *lse, const da_launch_opts *opts);
@@ -68,7 +67,7 @@ int check_desc(const da_desc *d) {
             break;
         case DA_KV_FP8_MLA656:
             if (d->H_kv != 1 || d->D_qk != 576 || d->D_v != 512 || d->G != 128) return DA_ERR_UNSUPPORTED;
-            if (sq != 1 || d->window != 0) return DA_ERR_UNSUPPORTED;
+            if (sq > kMaxSqMla || d->window != 0 || (d->topk > 0 && sq != 1)) return DA_ERR_UNSUPPORTED;
             if (!mla_kernel_available()) return DA_ERR_UNSUPPORTED;
             break;
         default:
@@ -85,13 +84,6 @@ int resolve_sms(const da_desc *d, int *nsm) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
     if (cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DA_ERR_CUDA;
-    if (is_mla(d)) {
-        // the latent-token kernel runs as two-CTA clusters: count the SMs that
-        // can hold one at the same time
-        const int clusters = mla_max_parts();
-        if (clusters < 1) return DA_ERR_CUDA;
-        if (2 * clusters < *nsm) *nsm = 2 * clusters;
-    }
     return DA_OK;
 }
 
@@ -102,7 +94,7 @@ int32_t g_page_trace_cap = 0;
 uint64_t g_wait_limit_ns = 0;  // 0: kWaitLimitNs
 int32_t g_debug_stall = 0;
 
-int cpc_of(const da_desc *d) { return is_mla(d) ? mla_ctas_per_part() : 1; }
+int cpc_of(const da_desc *d) { return is_mla(d) ? mla_ctas_per_part(sq_of(d)) : 1; }
 
 int make_layout(const da_desc *d, MetaLayout *L) {
     int rc = check_desc(d);
@@ -139,8 +131,6 @@ int make_layout(const da_desc *d, MetaLayout *L) {
     off += round_up((size_t)max_splits * rows * 4, 256);
     L->o_part = off;
     off += round_up((size_t)max_splits * rows * d->D_v * 4, 256);
-    L->xchg = off;  // per part, per CTA of the pair: 128 heads x 64 tokens fp32
-    if (is_mla(d)) off += round_up((size_t)num_parts * 2 * H_q * kChunk * 4, 256);
     L->total = off;
     L->num_parts = (int32_t)num_parts;
     L->max_splits = (int32_t)max_splits;
@@ -158,7 +148,6 @@ MetaView meta_view(void *meta, const MetaLayout &L) {
     v.num_splits = reinterpret_cast<const int32_t *>(base + L.num_splits);
     v.lse_part = reinterpret_cast<float *>(base + L.lse_part);
     v.o_part = reinterpret_cast<float *>(base + L.o_part);
-    v.xchg = reinterpret_cast<float *>(base + L.xchg);
     v.max_splits = L.max_splits;
     return v;
 }
@@ -428,6 +417,8 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.page_trace_cap = g_page_trace_cap;
         p.indices = desc->topk > 0 ? indices : nullptr;
         p.topk = desc->topk;
+        p.s_q = sq_of(desc);
+        p.debug_stall = g_debug_stall;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     }

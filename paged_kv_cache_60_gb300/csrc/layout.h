@@ -12,6 +12,7 @@ constexpr int32_t kMetaMagic = 0x44414d31;  // "DAM1"
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kMaxSqD64 = 4;               // query tokens per request: bf16 D = 64 kernel
 constexpr int kMaxSqD128 = 4;              // bf16 / e4m3 D = 128 kernels
+constexpr int kMaxSqMla = 4;               // 656-byte latent format (one CTA pair per query token)
 
 // sched_meta header words
 enum MetaHeader : int {
@@ -46,7 +47,7 @@ struct PartRec {
 constexpr int kPartRecInts = 8;
 
 struct MetaLayout {
-    size_t header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part, xchg, total;
+    size_t header, parts, chunk_offset, split_offset, num_splits, lse_part, o_part, total;
     int32_t num_parts, max_splits, cpc;
 };
 
@@ -59,7 +60,6 @@ struct MetaView {
     const int32_t *num_splits;
     float *lse_part;   // [max_splits][s_q * H_q]
     float *o_part;     // [max_splits][s_q * H_q][D_v]
-    float *xchg;       // latent-token kernel only: partial scores swapped between the CTAs of a part
     int32_t max_splits;
 };
 
@@ -117,14 +117,15 @@ struct GqaParams {
 };
 
 struct MlaParams {
-    const void *q;                 // bf16 [B][H_q][576]
+    const void *q;                 // bf16 [B][s_q][H_q][576]
     const uint8_t *pool;           // 656-byte tokens
     const int32_t *block_table;
     const int32_t *seqlens;
     MetaView meta;
-    void *out;                     // bf16 [B][H_q][512]
-    float *lse;
+    void *out;                     // bf16 [B][s_q][H_q][512]
+    float *lse;                    // [B][s_q][H_q]
     int32_t B, H_q, max_pages, num_pages, page_size;
+    int32_t s_q;                   // query tokens per request (draft j sees L - s_q + 1 + j tokens)
     int32_t splits, num_parts;
     float scale_log2;
     uint64_t wait_limit_ns;
@@ -132,6 +133,7 @@ struct MlaParams {
     int32_t page_trace_cap;        // chunks recorded per part
     const int32_t *indices;        // sparse decode: [B][topk] token positions, or null
     int32_t topk;                  // 0: dense (tokens [0, L_b))
+    int32_t debug_stall;           // test build only: the softmax warps first wait on a barrier nothing completes
 };
 
 struct CombineParams {

@@ -2,6 +2,8 @@
 KV head, D_qk = 576, D_v = 512): the tensor-core kernel through the C ABI
 against the float64 oracle. Metadata bit-exact (two CTAs per part), lse within
 1e-4, out within 2e-2."""
+import dataclasses
+
 import pytest
 import torch
 
@@ -24,13 +26,9 @@ def _built():
 
 
 def _auto_sms(desc):
-    """SM count the auto partition was built for: the library counts only the
-    SMs that can hold its two-CTA clusters at the same time."""
-    if desc.splits > 0:
-        return device_sms()
-    n = da.num_parts(desc)
-    assert 1 <= 2 * n <= device_sms()
-    return 2 * n
+    """SM count the auto partition was built for: every SM of the device
+    (2 s_q CTAs per part, one per SM)."""
+    return device_sms()
 
 
 def _mla(**kw):
@@ -92,6 +90,64 @@ def test_mla_repeat_bitwise():
     o2, l2, _, _ = run(w)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ------------------------------------------------------------------ several query tokens (drafts)
+
+MULTI = [
+    dict(s_q=2),
+    dict(s_q=2, splits=3),
+    dict(s_q=2, lengths=[1, 2, 64, 65, 129, 0]),
+    dict(s_q=2, lengths=[2500, 90], page_size=32, splits=4),
+    dict(s_q=3, lengths=[700, 3, 1300]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(MULTI)))
+def test_mla_multitoken_parity(case):
+    """s_q query tokens per request on the latent format: one CTA pair per
+    draft, draft j seeing the first L - s_q + 1 + j tokens; against the
+    oracle's masked decode step, with the schedule bit-exact (2 s_q CTAs per
+    part)."""
+    kw = MULTI[case]
+    w = make_workload(_mla(**kw))
+    out, lse, meta, desc = run(w)
+    torch.cuda.synchronize()
+    assert da.get_error(meta) == 0
+    sq = kw["s_q"]
+    got = read_meta(meta, desc)
+    ref = sched_ref(w.lengths, 1, w.spec.splits, device_sms(), cpc=2 * sq, s_q=sq)
+    assert got["parts"] == ref.parts
+    ref_out, ref_lse = oracle.attend_multi(w)
+    e_out, e_lse = max_err(out.view(ref_out.shape), lse.view(ref_lse.shape), ref_out, ref_lse)
+    assert e_out <= OUT_TOL, (kw, e_out)
+    assert e_lse <= LSE_TOL, (kw, e_lse)
+
+
+def test_mla_last_draft_matches_single_token():
+    """The last of two drafts sees every token: it equals the one-token call on
+    the same pool (same kernel arithmetic, same partition shape per CTA pair)."""
+    w = make_workload(_mla(s_q=2, lengths=[1500, 333, 64], splits=2))
+    out, lse, _, _ = run(w)
+    single = dataclasses.replace(w, spec=w.spec.with_(s_q=1), q=w.q[:, -1].contiguous())
+    o1, l1, _, _ = run(single)
+    torch.cuda.synchronize()
+    assert torch.equal(out[:, -1], o1) and torch.equal(lse[:, -1], l1)
+
+
+def test_mla_multitoken_workload_parity():
+    """The latent workload with two query tokens per request (spec2_mla_fp8),
+    full launch; every request against the oracle."""
+    w = make_workload(spec_by_name("spec2_mla_fp8"))
+    out, lse, meta, desc = run(w)
+    torch.cuda.synchronize()
+    assert da.get_error(meta) == 0
+    ref_out, ref_lse = oracle.attend_multi(w)
+    assert not torch.isnan(ref_lse).any()
+    e_out, e_lse = max_err(out.view(ref_out.shape), lse.view(ref_lse.shape), ref_out, ref_lse)
+    assert e_out <= OUT_TOL, e_out
+    assert e_lse <= LSE_TOL, e_lse
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
 
 
 def test_mla_bad_page_sets_error_word():

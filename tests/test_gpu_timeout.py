@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import paged_kv_cache_60_gb300 as da
-from workloads import KV_BF16, KV_FP8, WorkloadSpec, make_workload
+from workloads import KV_BF16, KV_FP8, KV_MLA656, WorkloadSpec, make_workload
 
 from gpu_util import LSE_TOL, OUT_TOL, DeviceWorkload, debug_build_library, make_desc, max_err
 
@@ -55,6 +55,30 @@ def test_wait_that_runs_out_sets_timeout_and_context_survives(tlib, kv):
         tlib.decode_attn_debug_wait_limit(0)
     assert err & da.DA_DEV_TIMEOUT, err
     # the context is still usable and the normal bound gives the oracle's result
+    out, lse, err = _call(tlib, w, dw, desc)
+    assert err == 0
+    ref_out, ref_lse = oracle.attend(w)
+    e_out, e_lse = max_err(out, lse, ref_out, ref_lse)
+    assert e_out <= OUT_TOL and e_lse <= LSE_TOL, (e_out, e_lse)
+
+
+def test_latent_kernel_wait_that_runs_out(tlib):
+    """The same on the 656-byte latent format: its CTAs never read each
+    other's memory, so a CTA that gives up leaves nothing in flight; the MMA
+    warp drains what it issued before the tensor memory is freed."""
+    spec = WorkloadSpec(name="t", B=3, H_kv=1, G=128, D_qk=576, D_v=512, page_size=64, kv_dtype=KV_MLA656,
+                        lengths=[3000, 700, 1500], splits=0, seed=52)
+    w = make_workload(spec)
+    dw = DeviceWorkload(w)
+    desc = make_desc(w)
+    assert tlib.decode_attn_debug_wait_limit(1000000) == 0
+    assert tlib.decode_attn_debug_stall(1) == 0
+    try:
+        _, _, err = _call(tlib, w, dw, desc)
+    finally:
+        tlib.decode_attn_debug_stall(0)
+        tlib.decode_attn_debug_wait_limit(0)
+    assert err & da.DA_DEV_TIMEOUT, err
     out, lse, err = _call(tlib, w, dw, desc)
     assert err == 0
     ref_out, ref_lse = oracle.attend(w)

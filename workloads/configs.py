@@ -95,6 +95,14 @@ CONFIGS = [
         name="window_sinks_gqa_bf16", B=32, H_kv=8, G=8, D_qk=128, D_v=128, page_size=64,
         length_dist="uniform", length_lo=1024, length_hi=8192, splits=0, seed=1008, window=2048, sinks=True,
         description="B=32 H_q=64 H_kv=8 D=128 P=64 L~U[1024,8192] sliding window 2048, one sink per head"),
+    # the latent-token workload with two query tokens per request (FlashMLA's call
+    # passes s_q * h_q / h_kv rows per KV head; no page gives a number for it)
+    WorkloadSpec(
+        name="spec2_mla_fp8", B=32, H_kv=1, G=128, D_qk=576, D_v=512, page_size=64,
+        kv_dtype=KV_MLA656, length_dist="loguniform", length_lo=4096, length_hi=131072,
+        splits=0, seed=1011, s_q=2,
+        description="B=32 s_q=2 H_q=128 H_kv=1 D_qk=576 D_v=512 P=64 656-byte FP8 tokens, "
+                    "L log-uniform [4096,131072], draft chain of 2"),
     # sparse top-k decode on the latent-token format: the pages' "FP8 稀疏解码" row
     # (topk 2048, batch 128, 128 heads); the context length is not given there
     WorkloadSpec(
