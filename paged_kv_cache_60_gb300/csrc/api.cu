@@ -19,6 +19,7 @@ cudaError_t launch_combine(int DV, const CombineParams &p, cudaStream_t stream, 
 cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stream, bool pdl);
 int mla_ctas_per_part(int s_q);
 bool mla_kernel_available();
+int mla_max_parts(int s_q);
 int check_fwd_args(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
                    const float *k_scale, const float *v_scale, const int32_t *block_table,
                    const int32_t *cache_seqlens, const void *out, const float *lse, const da_launch_opts *opts);
@@ -84,6 +85,14 @@ int resolve_sms(const da_desc *d, int *nsm) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
     if (cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DA_ERR_CUDA;
+    if (is_mla(d)) {
+        // the latent-token kernel runs as clusters of 2 s_q CTAs: count the SMs
+        // that can hold them at the same time
+        const int cpc = mla_ctas_per_part(sq_of(d));
+        const int clusters = mla_max_parts(sq_of(d));
+        if (clusters < 1) return DA_ERR_CUDA;
+        if (cpc * clusters < *nsm) *nsm = cpc * clusters;
+    }
     return DA_OK;
 }
 
@@ -240,7 +249,7 @@ int da::check_fwd_args(const da_desc *desc, const void *q, const void *k_pool, c
     const int32_t *indices = opts ? opts->indices : nullptr;
     if (desc->topk > 0 && !indices) return DA_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(indices) & 3u) return DA_ERR_ALIGN;
-    if (!mla && (int64_t)desc->page_size * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
+    if ((int64_t)desc->page_size * desc->num_pages > (int64_t)INT32_MAX) return DA_ERR_DIMS;
     return DA_OK;
 }
 
@@ -419,6 +428,9 @@ int decode_attn_fwd_ex(const da_desc *desc, const void *q, const void *k_pool, c
         p.topk = desc->topk;
         p.s_q = sq_of(desc);
         p.debug_stall = g_debug_stall;
+        p.log2_page = -1;
+        for (int k = 0; k < 31; ++k)
+            if (desc->page_size == (1 << k)) p.log2_page = k;
         if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return DA_ERR_CUDA;
         if (launch_mla(p, stream, pdl) != cudaSuccess) return DA_ERR_CUDA;
     }

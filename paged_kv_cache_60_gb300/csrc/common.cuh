@@ -145,6 +145,40 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, c
     }
 }
 
+// The same with the first poll inline and the rest out of line (keeps the
+// callers' code small).
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (up to `ns`) until it is, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+static __device__ __noinline__ bool mbar_wait_warp_slow(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                                 uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 20000u))) return true;
+        if ((it & 3) == 3) {
+            int stop = (*abort != 0) || (global_ns() - t0 > limit_ns);
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_wait_warp_ool(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                                   uint64_t limit_ns) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    return mbar_wait_warp_slow(bar, parity, abort, limit_ns);
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -222,6 +256,11 @@ __device__ __forceinline__ float ldg_stream4f(const void *ptr) {
     float v;
     asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
     return v;
+}
+// Bring `bytes` (a multiple of 16, from a 16-byte aligned address) into L2
+// without waiting: the loads that follow hit L2 instead of HBM.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     uint32_t y;

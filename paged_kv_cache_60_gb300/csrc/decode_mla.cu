@@ -42,6 +42,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "decode_attn.h"
 #include "segwalk.cuh"
@@ -95,51 +97,38 @@ constexpr float kLn2Mla = 0.6931471805599453f;
 
 __device__ __forceinline__ uint32_t swz(int row, int c16) { return (uint32_t)(row * 128 + ((c16 ^ (row & 7)) << 4)); }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float mul_rn(float a, float b) {
     float r;
     asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
 }
 
-// Exact e4m3 -> fp32 without the conversion pipe, for the code in bits
-// [24, 32) of x: an arithmetic shift by 4 puts its exponent and mantissa on
-// fp32 bits 20-26 and copies its sign onto bits 27-31; the mask keeps bits
-// 20-26 and the sign at bit 31. The pattern is the code's value times
-// 2^-120 (an fp32 subnormal for e4m3 subnormals). The NaN codes (0x7f, 0xff)
-// read as +-480 here; the tokens a decode step reads never hold them.
-__device__ __forceinline__ float e4m3_top_scaled(uint32_t x) {
-    return __uint_as_float((uint32_t)((int32_t)x >> 4) & 0x87F00000u);
-}
-
-// 16 e4m3 values times `scale` (one fp32 rounding of the exact product, then
-// bf16 round to nearest even), as 16 bf16 (two 16-byte words). For scales
-// below 2^8 the 2^120 that the bit moves leave out is folded into the scale
-// (scale * 2^120 is exact), so one multiply gives RN(e4m3 * scale); larger or
-// non-finite scales take a second, exact multiply by 2^120 first.
+// 16 e4m3 values times `scale`, as 16 bf16 (two 16-byte words): each code goes
+// to f16 by the hardware pair conversion (exact: every e4m3 value, NaN
+// included, is an f16 value), then to fp32 (exact), is multiplied by the scale
+// in fp32 (one rounding of the exact product) and rounded to bf16 (nearest
+// even) -- the FlashMLA page's chain (section 计算环节一: FP8 -> half -> float32,
+// times the scale, -> bfloat16).
 __device__ __forceinline__ void dequant16(const uint4 v, float scale, uint4 &lo, uint4 &hi) {
-    const float two120 = __uint_as_float(0x7B800000u);
-    const bool folded = scale < 256.f;
-    const float m = folded ? mul_rn(scale, two120) : scale;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float f[16];
+    uint32_t o[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint32_t x = w[k];
-        f[4 * k] = e4m3_top_scaled(x << 24);
-        f[4 * k + 1] = e4m3_top_scaled(x << 16);
-        f[4 * k + 2] = e4m3_top_scaled(x << 8);
-        f[4 * k + 3] = e4m3_top_scaled(x);
+        const uint32_t h01 = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xFFFFu));
+        const uint32_t h23 = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+        o[2 * k] = pack_bf16(mul_rn(a.x, scale), mul_rn(a.y, scale));
+        o[2 * k + 1] = pack_bf16(mul_rn(b.x, scale), mul_rn(b.y, scale));
     }
-    if (folded) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) f[e] = mul_rn(f[e], m);
-    } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) f[e] = mul_rn(mul_rn(f[e], two120), m);
-    }
-    lo = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-    hi = make_uint4(pack_bf16(f[8], f[9]), pack_bf16(f[10], f[11]), pack_bf16(f[12], f[13]),
-                    pack_bf16(f[14], f[15]));
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // Slice s of a latent row in this CTA's rings: the value slot holds slices
@@ -154,18 +143,21 @@ template <int R, bool KONLY>
 __device__ __forceinline__ void mla_issue_qk(uint32_t tmem, uint64_t dq0, uint64_t dslot) {
     using namespace mla;
     constexpr uint32_t IDESC_QK = umma_idesc_bf16(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
     for (int k = 0; k < (KONLY ? KSL : VSL); ++k) {
         const int s = KONLY ? (R == 0 ? 4 + k : (k < 4 ? k : 8)) : 4 * R + k;
+        const uint64_t db = dslot + (uint64_t)((k * SLICE) >> 4);
+        // a 16-dim step advances both descriptors by 32 bytes (2 units of 16 bytes)
+        if (s < QTM) {
+            const uint32_t a = tmem + Q_COL + 32 * s;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint64_t db = dslot + (uint64_t)((k * SLICE + 32 * i) >> 4);
-            const bool acc = !(KONLY && k == 0 && i == 0);
-            if (s < QTM)
-                umma_bf16_tmem_a_w(tmem + S_COL, tmem + Q_COL + 32 * s + 8 * i, db, IDESC_QK, acc);
-            else
-                umma_bf16_ss_w(tmem + S_COL, dq0 + (uint64_t)(((s - QTM) * QSLICE + 32 * i) >> 4), db, IDESC_QK,
-                               acc);
+            for (int i = 0; i < 4; ++i)
+                umma_bf16_tmem_a_w(tmem + S_COL, a + 8 * i, db + 2 * i, IDESC_QK, !(KONLY && k == 0 && i == 0));
+        } else {
+            const uint64_t da = dq0 + (uint64_t)(((s - QTM) * QSLICE) >> 4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                umma_bf16_ss_w(tmem + S_COL, da + 2 * i, db + 2 * i, IDESC_QK, !(KONLY && k == 0 && i == 0));
         }
     }
 }
@@ -195,7 +187,7 @@ __device__ __noinline__ void mla_issue(const MlaParams &p, uint8_t *smem, uint32
     int cur = 0, nseg = 0;
     int pend = -1, pend_first = 0, pend_last = 0, pend_seg = 0;
     auto wait = [&](uint64_t *bar, uint32_t par) -> bool {
-        return ok && (ok = mbar_wait_warp(bar, par, abort_flag, p.wait_limit_ns));
+        return ok && (ok = mbar_wait_warp_ool(bar, par, abort_flag, p.wait_limit_ns));
     };
     // O[:, value dims] += P(x) V(x)
     auto issue_pv = [&](int x, bool first, bool last, int seg) {
@@ -316,113 +308,255 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     } else if (warp >= 1 + SM_WARPS) {
         // ------------------------------------------------------------ dequantise whole rows
         // A row is 40 units of 16 bytes: 32 of NoPE codes (16 values, the scale of
-        // their 128-value block), 8 of RoPE values (8 bf16, copied as stored). Per
-        // chunk, the 24 units per row that only Q K^T reads (16 NoPE, 8 RoPE) are
-        // loaded, converted and stored first; then the 16 units of this CTA's
-        // value dims. Thread dt takes units dt + 256 i of each kind, so a warp's
-        // loads cover contiguous bytes of one or two rows.
+        // their 128-value block), 8 of RoPE values (8 bf16, copied as stored).
+        // Thread dt owns NoPE column gk = 16 (1 - r) + dt % 16 (read by Q K^T only)
+        // and gv = 16 r + dt % 16 (a value column) of tokens dt / 16 + 16 i (i < 4),
+        // and RoPE unit 32 + dt % 8 of tokens dt / 8 + 32 j (j < 2): per chunk four
+        // K-only NoPE units, four value units and two RoPE units, the same kind of
+        // work on every lane. A warp's loads cover 256 contiguous bytes of two rows.
+        // Within a segment the work is software-pipelined: the block-table lookups
+        // of chunk c + 2 (and the L2 prefetch of its rows), the loads of the value
+        // units of chunk c before its K-only units are converted, and the loads of
+        // the K-only units of chunk c + 1 before the value units of c are.
         const int dt = threadIdx.x - (1 + SM_WARPS) * 32;  // 0 .. 255
+        const int gk = 16 * (1 - r) + (dt & 15), gv = 16 * r + (dt & 15), gr = dt & 7;
+        const bool pf_lane = (dt & 15) == 0;               // these 16 threads cover the 64 rows of a chunk
+        auto tok_of = [&](int k) { return k < 4 ? (dt >> 4) + 16 * k : (dt >> 3) + 32 * (k - 4); };
+        // Where this thread's units land in a slot: token rows dt / 16 + 16 i share
+        // their swizzle (token & 7), so the offsets of the two 16-byte chunks of a
+        // NoPE unit are fixed per thread (+ 2048 i for unit i); odd slices store the
+        // upper chunk first (fewer bank conflicts).
+        auto nope_off = [&](int g, int base, int half) -> uint32_t {
+            const int tok = dt >> 4, c0 = 2 * (g & 3), swap = (g >> 2) & 1;
+            return base + swz(tok, c0 + (half ^ swap));
+        };
+        const uint32_t k_lo = nope_off(gk, OFF_K + k_slot_index(gk >> 2, r) * SLICE, 0);
+        const uint32_t k_hi = nope_off(gk, OFF_K + k_slot_index(gk >> 2, r) * SLICE, 1);
+        const uint32_t v_lo = nope_off(gv, OFF_V + ((gv >> 2) - 4 * r) * SLICE, 0);
+        const uint32_t v_hi = nope_off(gv, OFF_V + ((gv >> 2) - 4 * r) * SLICE, 1);
+        const uint32_t r_off = OFF_K + k_slot_index(8, r) * SLICE + swz(dt >> 3, gr);  // + 4096 j
+        const bool kswap = (gk >> 2) & 1, vswap = (gv >> 2) & 1;
+        // 16 e4m3 codes -> 16 bf16, the first store at byte offset o_1 of shared
+        // memory (chunk c0 + swap), the second at o_2; with swap the upper 8 codes
+        // are converted into the first word
+        auto store_nope = [&](uint32_t o_1, uint32_t o_2, bool swap, uint4 v, float sc) {
+            if (swap) v = make_uint4(v.z, v.w, v.x, v.y);
+            uint4 w1, w2;
+            dequant16(v, sc, w1, w2);
+            *reinterpret_cast<uint4 *>(smem + o_1) = w1;
+            *reinterpret_cast<uint4 *>(smem + o_2) = w2;
+        };
+        auto load_nope = [&](int row, int g, uint4 &v, float &sc) {
+            v = make_uint4(0u, 0u, 0u, 0u);
+            sc = 0.f;
+            if (row < 0) return;
+            const uint8_t *base = p.pool + (size_t)row * ROW_BYTES;
+            v = ldg_stream16(base + 16 * g);
+            sc = ldg_stream4f(base + 512 + 4 * (g >> 3));
+        };
+        auto load_rope = [&](int row) -> uint4 {
+            return row < 0 ? make_uint4(0u, 0u, 0u, 0u) : ldg_stream16(p.pool + (size_t)row * ROW_BYTES + 528 + 16 * gr);
+        };
         SegWalker wk = make_walker(p.meta, rec0, rec1, p.B, p.seqlens, max_len, p.s_q, 0, p.topk);
         Seg sg;
         int cur = 0;
         bool ok = true;
-        uint8_t *const vring = smem + OFF_V;
-        uint8_t *const kring = smem + OFF_K;
         while (ok && wk.next(sg)) {
             const int n = sg.lc1 - sg.lc0;
+            if (n == 0) continue;
             const int32_t *bt_row = p.block_table + (size_t)sg.b * p.max_pages;
             const int32_t *idx_row = p.indices + (size_t)sg.b * p.topk;  // sparse decode only
-            // one unit: its 16 bytes of the row of position t (zero when t is outside
-            // the sequence or its page outside the pool) and, for NoPE, its scale
-            auto load_unit = [&](int t, int g, uint4 &v, float &sc) {
-                v = make_uint4(0u, 0u, 0u, 0u);
-                sc = 0.f;
-                if (t < 0 || t >= sg.L) return;
-                const int pg = bt_row[t / p.page_size];
+            // position of token `tok` of local chunk cc: dense, the token itself; sparse,
+            // the position listed in that slot; -1 past the segment, past topk or
+            // outside [0, L) (a zero row)
+            auto position = [&](int cc, int tok) -> int {
+                if (cc >= n) return -1;
+                const int s = (sg.lc0 + cc) * kChunk + tok;
+                int t = s;
+                if (SPARSE) t = s < p.topk ? idx_row[s] : -1;
+                return (t >= 0 && t < sg.L) ? t : -1;
+            };
+            auto page_index = [&](int t) -> int { return p.log2_page >= 0 ? t >> p.log2_page : t / p.page_size; };
+            // Dense decode reads the block table through a window of 64 entries,
+            // [wbase, wbase + 64), two per lane (wcur: wbase + lane, wnext: wbase + 32 +
+            // lane), loaded a window ahead: page lookups are warp shuffles, without the
+            // latency of a load (the table's lines leave L2 between uses under the row
+            // stream). Entries past the request's pages are not read (-1).
+            const int npg = (sg.L + p.page_size - 1) / p.page_size;
+            auto bt_load = [&](int i) -> int { return i < npg ? bt_row[i] : -1; };
+            int wbase = 0, wcur = -1, wnext = -1;
+            if (!SPARSE) {
+                wbase = page_index(sg.lc0 * kChunk) & ~31;
+                wcur = bt_load(wbase + lane);
+                wnext = bt_load(wbase + 32 + lane);
+            }
+            // slides the window on until index lo lies in its first half (every lane)
+            auto advance = [&](int lo) {
+                while (lo >= wbase + 32) {
+                    wbase += 32;
+                    wcur = wnext;
+                    wnext = bt_load(wbase + 32 + lane);
+                }
+            };
+            // page of position t (every lane of the warp calls it: shuffles)
+            auto page_of = [&](int t) -> int {
+                if (SPARSE) return t < 0 ? -1 : bt_row[page_index(t)];
+                const int i = t < 0 ? wbase : page_index(t);
+                const int a = __shfl_sync(0xffffffffu, wcur, (i - wbase) & 31);
+                const int b = __shfl_sync(0xffffffffu, wnext, (i - wbase) & 31);
+                return t < 0 ? -1 : (i - wbase < 32 ? a : b);
+            };
+            // pool row of position t on page pg, or -1 (a page outside the pool sets the error bit)
+            auto row_of = [&](int t, int pg) -> int {
+                if (t < 0) return -1;
                 if (pg < 0 || pg >= p.num_pages) {
                     atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
                     p.meta.header[kHErrorDetail] = pg;
-                    return;
+                    return -1;
                 }
-                const uint8_t *row = p.pool + ((size_t)pg * p.page_size + t % p.page_size) * ROW_BYTES;
-                if (g >= 32) {
-                    v = ldg_stream16(row + 528 + 16 * (g - 32));
-                } else {
-                    v = ldg_stream16(row + 16 * g);
-                    sc = ldg_stream4f(row + 512 + 4 * (g >> 3));
-                }
+                return pg * p.page_size + (p.log2_page >= 0 ? t & (p.page_size - 1) : t % p.page_size);
             };
-            // converts (NoPE) or copies (RoPE) one unit into its slice of a tile
-            auto store_unit = [&](uint8_t *slice, int tok, int g, const uint4 v, float sc) {
-                if (g >= 32) {  // 16-byte chunk g - 32 of slice 8, as stored
-                    *reinterpret_cast<uint4 *>(slice + swz(tok, g - 32)) = v;
-                    return;
+            // rows of this thread's tokens in local chunk cc, dense decode with pages
+            // of at least one chunk: one page per chunk, no memory latency
+            auto chunk_rows_dense = [&](int cc, int rows[6]) {
+                const int t0 = (sg.lc0 + cc) * kChunk;
+                const bool in = cc < n;
+                const int pg = page_of(in ? t0 : -1);
+                const bool pg_ok = pg >= 0 && pg < p.num_pages;
+                if (in && !pg_ok) {
+                    atomicOr(&p.meta.header[kHError], DA_DEV_BAD_PAGE);
+                    p.meta.header[kHErrorDetail] = pg;
                 }
-                uint4 lo, hi;
-                dequant16(v, sc, lo, hi);
-                // 16-byte chunks c0, c0 + 1 of the slice's row; odd slices store the
-                // upper chunk first (fewer bank conflicts across the warp)
-                const int c0 = 2 * (g & 3);
-                const bool swap = (g >> 2) & 1;
-                *reinterpret_cast<uint4 *>(slice + swz(tok, c0 + (swap ? 1 : 0))) = swap ? hi : lo;
-                *reinterpret_cast<uint4 *>(slice + swz(tok, c0 + (swap ? 0 : 1))) = swap ? lo : hi;
+                const int rb = pg * p.page_size + (p.log2_page >= 0 ? t0 & (p.page_size - 1) : t0 % p.page_size);
+#pragma unroll
+                for (int k = 0; k < 6; ++k)
+                    rows[k] = (in && pg_ok && t0 + tok_of(k) < sg.L) ? rb + tok_of(k) : -1;
             };
+            const bool one_page = !SPARSE && p.page_size >= kChunk;
+            int pos2[6], row0[6], row1[6];
+            // prologue: rows of chunks 0 and 1 (prefetched), positions of chunk 2
+            if (one_page) {
+                chunk_rows_dense(0, row0);
+                chunk_rows_dense(1, row1);
+#ifdef DA_PAGE_TRACE
+                if (p.page_trace && blockIdx.y == 0 && pf_lane) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (cur < p.page_trace_cap)
+                            p.page_trace[((size_t)part * p.page_trace_cap + cur) * kChunk + tok_of(k)] =
+                                row0[k] >= 0 ? row0[k] : -2;
+                        if (n > 1 && cur + 1 < p.page_trace_cap)
+                            p.page_trace[((size_t)part * p.page_trace_cap + cur + 1) * kChunk + tok_of(k)] =
+                                row1[k] >= 0 ? row1[k] : -2;
+                    }
+                }
+#endif
+            } else
+#pragma unroll
+            for (int k = 0; k < 6; ++k) {
+                const int t0 = position(0, tok_of(k)), t1 = position(1, tok_of(k));
+                const int pg0 = page_of(t0), pg1 = page_of(t1);
+                row0[k] = row_of(t0, pg0);
+                row1[k] = row_of(t1, pg1);
+                pos2[k] = position(2, tok_of(k));
+#ifdef DA_PAGE_TRACE
+                if (p.page_trace && blockIdx.y == 0 && pf_lane && k < 4) {
+                    if (cur < p.page_trace_cap)
+                        p.page_trace[((size_t)part * p.page_trace_cap + cur) * kChunk + tok_of(k)] =
+                            t0 >= 0 ? pg0 * p.page_size + t0 % p.page_size : -2;
+                    if (n > 1 && cur + 1 < p.page_trace_cap)
+                        p.page_trace[((size_t)part * p.page_trace_cap + cur + 1) * kChunk + tok_of(k)] =
+                            t1 >= 0 ? pg1 * p.page_size + t1 % p.page_size : -2;
+                }
+#endif
+            }
+            if (pf_lane) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (row0[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row0[k] * ROW_BYTES, ROW_BYTES);
+                    if (row1[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row1[k] * ROW_BYTES, ROW_BYTES);
+                }
+            }
+            uint4 kn[4], kr[2];
+            float ksc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) load_nope(row0[i], gk, kn[i], ksc[i]);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) kr[j] = load_rope(row0[4 + j]);
             for (int c = 0; c < n && ok; ++c, ++cur) {
                 const int slot = cur % NR;
                 const uint32_t par = ((cur / NR) & 1) ^ 1;
-                const int tbase = (sg.lc0 + c) * kChunk;
-                // dense: token tbase + tok; sparse: the position listed in slot tbase + tok
-                // (slots past topk and positions outside [0, L) are skipped: a zero row)
-                auto position = [&](int tok) -> int {
-                    if (!SPARSE) return tbase + tok;
-                    return tbase + tok < p.topk ? idx_row[tbase + tok] : -1;
-                };
-                {
-                    uint4 v[KUPT];
-                    float sc[KUPT];
+                // a. block-table lookups of chunk c + 2
+                if (!SPARSE && c + 2 < n) advance(page_index((sg.lc0 + c + 2) * kChunk));
+                int pg2[6];
+                if (!one_page) {
 #pragma unroll
-                    for (int i = 0; i < KUPT; ++i) {
-                        const int u = dt + DQ_THREADS * i, tok = u / KU, kg = u % KU;
-                        const int g = kg < 16 ? 16 * (1 - r) + kg : 16 + kg;
-                        const int t = position(tok);
-#ifdef DA_PAGE_TRACE
-                        if (p.page_trace && blockIdx.y == 0 && kg == 0 && cur < p.page_trace_cap)
-                            p.page_trace[((size_t)part * p.page_trace_cap + cur) * kChunk + tok] =
-                                (t >= 0 && t < sg.L) ? bt_row[t / p.page_size] * p.page_size + t % p.page_size : -2;
-#endif
-                        load_unit(t, g, v[i], sc[i]);
-                    }
-                    // the K-only slots are free once Q K^T of the chunk two back has read them
-                    if (!(ok = mbar_wait_warp(&kempty[slot], par, abort_flag, p.wait_limit_ns))) break;
-#pragma unroll
-                    for (int i = 0; i < KUPT; ++i) {
-                        const int u = dt + DQ_THREADS * i, tok = u / KU, kg = u % KU;
-                        const int g = kg < 16 ? 16 * (1 - r) + kg : 16 + kg;
-                        const int s = g < 32 ? g >> 2 : 8;
-                        store_unit(kring + slot * KSLOT + k_slot_index(s, r) * SLICE, tok, g, v[i], sc[i]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&kfull[slot]);
+                    for (int k = 0; k < 6; ++k) pg2[k] = page_of(pos2[k]);
                 }
-                {
-                    uint4 v[VUPT];
-                    float sc[VUPT];
+                // b. loads of the value units of chunk c
+                uint4 vn[4];
+                float vsc[4];
 #pragma unroll
-                    for (int i = 0; i < VUPT; ++i) {
-                        const int u = dt + DQ_THREADS * i, tok = u / VU;
-                        load_unit(position(tok), 16 * r + u % VU, v[i], sc[i]);
-                    }
-                    // the value slots once P V of that chunk has read them
-                    if (!(ok = mbar_wait_warp(&vempty[slot], par, abort_flag, p.wait_limit_ns))) break;
+                for (int i = 0; i < 4; ++i) load_nope(row0[i], gv, vn[i], vsc[i]);
+                // c. the K-only units of chunk c, once Q K^T of the chunk two back has
+                // read the slot
+                if (!(ok = mbar_wait_warp_ool(&kempty[slot], par, abort_flag, p.wait_limit_ns))) break;
+                const uint32_t ks = slot * KSLOT;
 #pragma unroll
-                    for (int i = 0; i < VUPT; ++i) {
-                        const int u = dt + DQ_THREADS * i, tok = u / VU, g = 16 * r + u % VU;
-                        store_unit(vring + slot * VSLOT + ((g >> 2) - 4 * r) * SLICE, tok, g, v[i], sc[i]);
+                for (int i = 0; i < 4; ++i) store_nope(k_lo + ks + 2048 * i, k_hi + ks + 2048 * i, kswap, kn[i], ksc[i]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) *reinterpret_cast<uint4 *>(smem + r_off + ks + 4096 * j) = kr[j];
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kfull[slot]);
+                // d. rows of chunk c + 2 (into L2 now), positions of chunk c + 3
+                int row2[6];
+                if (one_page) {
+                    chunk_rows_dense(c + 2, row2);
+#ifdef DA_PAGE_TRACE
+                    if (p.page_trace && blockIdx.y == 0 && pf_lane && c + 2 < n && cur + 2 < p.page_trace_cap) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            p.page_trace[((size_t)part * p.page_trace_cap + cur + 2) * kChunk + tok_of(k)] =
+                                row2[k] >= 0 ? row2[k] : -2;
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&vfull[slot]);
+#endif
+                } else
+#pragma unroll
+                for (int k = 0; k < 6; ++k) {
+                    row2[k] = row_of(pos2[k], pg2[k]);
+#ifdef DA_PAGE_TRACE
+                    if (p.page_trace && blockIdx.y == 0 && pf_lane && k < 4 && c + 2 < n && cur + 2 < p.page_trace_cap)
+                        p.page_trace[((size_t)part * p.page_trace_cap + cur + 2) * kChunk + tok_of(k)] =
+                            pos2[k] >= 0 ? pg2[k] * p.page_size + pos2[k] % p.page_size : -2;
+#endif
+                }
+                if (pf_lane) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (row2[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row2[k] * ROW_BYTES, ROW_BYTES);
+                }
+                if (!one_page) {
+#pragma unroll
+                    for (int k = 0; k < 6; ++k) pos2[k] = position(c + 3, tok_of(k));
+                }
+                // e. loads of the K-only units of chunk c + 1
+#pragma unroll
+                for (int i = 0; i < 4; ++i) load_nope(row1[i], gk, kn[i], ksc[i]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) kr[j] = load_rope(row1[4 + j]);
+                // f. the value units of chunk c, once P V of the chunk two back has read the slot
+                if (!(ok = mbar_wait_warp_ool(&vempty[slot], par, abort_flag, p.wait_limit_ns))) break;
+                const uint32_t vs = slot * VSLOT;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) store_nope(v_lo + vs + 2048 * i, v_hi + vs + 2048 * i, vswap, vn[i], vsc[i]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&vfull[slot]);
+#pragma unroll
+                for (int k = 0; k < 6; ++k) {
+                    row0[k] = row1[k];
+                    row1[k] = row2[k];
                 }
             }
         }
@@ -441,7 +575,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         bool ok = true;
         if (p.debug_stall) {
             // test build only: a wait that nothing completes runs out
-            ok = mbar_wait_warp(stall, 0, abort_flag, p.wait_limit_ns);
+            ok = mbar_wait_warp_ool(stall, 0, abort_flag, p.wait_limit_ns);
             if (!ok && lane == 0) {
                 atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
                 *abort_flag = 1;
@@ -474,7 +608,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             }
             // this head's q row of query token `draft`: dims [0, 320) into tensor memory
             // (the A operand of its first five slices), dims [320, 576) into shared memory
-            if (!(ok = mbar_wait_warp(qfree, (nseg & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
+            if (!(ok = mbar_wait_warp_ool(qfree, (nseg & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
             {
                 const uint4 *qs = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                                                                  ((size_t)sg.b * rows + draft * HQ + head) * DQK);
@@ -513,7 +647,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     if (cbase + lane < p.topk) t0 = ir[lane];
                     if (cbase + lane + 32 < p.topk) t1 = ir[lane + 32];
                 }
-                bool w_ok = mbar_wait_warp(sfull, cur & 1, abort_flag, p.wait_limit_ns);
+                bool w_ok = mbar_wait_warp_ool(sfull, cur & 1, abort_flag, p.wait_limit_ns);
                 tc_fence_after();
                 float s[64];
                 {
@@ -525,28 +659,35 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sfree);
-                float mx = -INFINITY;
+                // raw scores of the tokens this query token does not see become -inf
                 if (SPARSE) {
                     // sparse: slot e counts when it lies before topk and lists a position in
                     // [0, L); the warp's ballots give the 64 bits (vm0: slots 0-31, vm1: 32-63)
                     const uint32_t vm0 = __ballot_sync(0xffffffffu, t0 >= 0 && t0 < sg.L);
                     const uint32_t vm1 = __ballot_sync(0xffffffffu, t1 >= 0 && t1 < sg.L);
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const bool v = ((e < 32 ? vm0 >> e : vm1 >> (e - 32)) & 1u) != 0u;
-                        s[e] = v ? s[e] * sl2 : -INFINITY;
-                        mx = fmaxf(mx, s[e]);
-                    }
+                    for (int e = 0; e < 64; ++e)
+                        if (!(((e < 32 ? vm0 >> e : vm1 >> (e - 32)) & 1u))) s[e] = -INFINITY;
                 } else {
                     const int nvalid = L_vis - cbase;  // tokens of this chunk the query token sees
+                    if (nvalid < kChunk) {             // the same for every thread of the CTA
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        s[e] = (e < nvalid) ? s[e] * sl2 : -INFINITY;
-                        mx = fmaxf(mx, s[e]);
+                        for (int e = 0; e < 64; ++e)
+                            if (e >= nvalid) s[e] = -INFINITY;
                     }
                 }
+                // sl2 = sigma log2(e) > 0: the max of the scaled scores is sl2 times the raw max
+                float m1[22];
+#pragma unroll
+                for (int e = 0; e < 21; ++e) m1[e] = fmax3(s[3 * e], s[3 * e + 1], s[3 * e + 2]);
+                m1[21] = s[63];
+                float m2[8];
+#pragma unroll
+                for (int e = 0; e < 7; ++e) m2[e] = fmax3(m1[3 * e], m1[3 * e + 1], m1[3 * e + 2]);
+                m2[7] = m1[21];
+                const float mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7])) * sl2;
                 // P's columns and O are free once the previous chunk's P V has completed
-                w_ok = w_ok && mbar_wait_warp(pfree, (cur & 1) ^ 1, abort_flag, p.wait_limit_ns);
+                w_ok = w_ok && mbar_wait_warp_ool(pfree, (cur & 1) ^ 1, abort_flag, p.wait_limit_ns);
                 if (__any_sync(0xffffffffu, !w_ok || *abort_flag != 0)) {
                     if (lane == 0) {
                         atomicOr(&p.meta.header[kHError], DA_DEV_TIMEOUT);
@@ -582,7 +723,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2(s[2 * e] - base), p1 = ex2(s[2 * e + 1] - base);
+                    const float p0 = ex2(fmaf(s[2 * e], sl2, -base)), p1 = ex2(fmaf(s[2 * e + 1], sl2, -base));
                     ps += p0 + p1;
                     pk[e] = pack_bf16(p0, p1);
                 }
@@ -604,7 +745,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             }
             if (!ok) break;
             // ---- epilogue: O / l for this CTA's 256 value dims of this head
-            const bool o_ok = mbar_wait_warp(ofull, nseg & 1, abort_flag, p.wait_limit_ns);
+            const bool o_ok = mbar_wait_warp_ool(ofull, nseg & 1, abort_flag, p.wait_limit_ns);
             tc_fence_after();
             if (o_ok) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -648,9 +789,37 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// CTAs per part: one pair (value-dim halves) per query token.
+// CTAs per part: one pair (value-dim halves) per query token. They form one
+// thread-block cluster, so they run on one GPC, in front of one L2 partition:
+// the rows the first CTA reads from HBM are L2 hits for the others.
 int mla_ctas_per_part(int s_q) { return 2 * s_q; }
 bool mla_kernel_available() { return true; }
+
+// Parts that can run at once: clusters of 2 s_q CTAs, one CTA per SM.
+int mla_max_parts(int s_q) {
+    static std::atomic<int> cached[64][kMaxSqMla + 1];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || s_q < 1 || s_q > kMaxSqMla) return 0;
+    if (const int c = cached[dev][s_q].load(std::memory_order_relaxed)) return c;
+    if (cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1024, 2 * s_q);
+    cfg.blockDim = dim3(mla::THREADS);
+    cfg.dynamicSmemBytes = mla::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 2 * s_q;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<false>, &cfg) != cudaSuccess) return 0;
+    cached[dev][s_q].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl) {
     auto kern = p.topk > 0 ? mla_decode_kernel<true> : mla_decode_kernel<false>;
@@ -661,11 +830,15 @@ cudaError_t launch_mla(const MlaParams &p, cudaStream_t stream, bool pdl) {
     cfg.blockDim = dim3(mla::THREADS);
     cfg.dynamicSmemBytes = mla::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 2 * p.s_q;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

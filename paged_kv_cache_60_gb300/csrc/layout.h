@@ -126,6 +126,7 @@ struct MlaParams {
     float *lse;                    // [B][s_q][H_q]
     int32_t B, H_q, max_pages, num_pages, page_size;
     int32_t s_q;                   // query tokens per request (draft j sees L - s_q + 1 + j tokens)
+    int32_t log2_page;             // log2(page_size) when it is a power of two, else -1
     int32_t splits, num_parts;
     float scale_log2;
     uint64_t wait_limit_ns;

@@ -26,9 +26,14 @@ def _built():
 
 
 def _auto_sms(desc):
-    """SM count the auto partition was built for: every SM of the device
-    (2 s_q CTAs per part, one per SM)."""
-    return device_sms()
+    """SM count the auto partition was built for: the library counts only the
+    SMs that can hold its clusters (2 s_q CTAs, one per SM) at the same time."""
+    cpc = 2 * max(1, desc.s_q)
+    if desc.splits > 0:
+        return device_sms()
+    n = da.num_parts(desc)
+    assert 1 <= cpc * n <= device_sms()
+    return cpc * n
 
 
 def _mla(**kw):
@@ -116,7 +121,7 @@ def test_mla_multitoken_parity(case):
     assert da.get_error(meta) == 0
     sq = kw["s_q"]
     got = read_meta(meta, desc)
-    ref = sched_ref(w.lengths, 1, w.spec.splits, device_sms(), cpc=2 * sq, s_q=sq)
+    ref = sched_ref(w.lengths, 1, w.spec.splits, _auto_sms(desc), cpc=2 * sq, s_q=sq)
     assert got["parts"] == ref.parts
     ref_out, ref_lse = oracle.attend_multi(w)
     e_out, e_lse = max_err(out.view(ref_out.shape), lse.view(ref_lse.shape), ref_out, ref_lse)
