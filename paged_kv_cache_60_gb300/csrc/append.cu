@@ -12,10 +12,12 @@
 //   * the 656-byte latent token (FlashMLA page, section "数据加载"): per block
 //     of 128 NoPE values, scale = max|x| / 448 (1 for an all-zero block),
 //     512 codes, the four fp32 scales, then the 64 RoPE values as bf16.
-// Rounding is the IEEE one everywhere: the quotient x / scale is an fp32
-// division rounded to nearest (not a multiply by a reciprocal), the e4m3 code
-// the nearest finite value with ties to even, saturating at +-448; NaN maps
-// to 0x7F. The pool layout is [num_pages][page_size][H_kv][D] (bf16 / e4m3)
+// Rounding is the IEEE one everywhere: the quotient x / scale is the fp32
+// division rounded to nearest (not a plain multiply by a reciprocal), the e4m3
+// code the nearest finite value with ties to even, saturating at +-448; NaN
+// maps to 0x7F. The quotient is computed by Markstein's correction of the
+// reciprocal product where that gives the rounded quotient exactly, and by the
+// division elsewhere (see quot_rn). The pool layout is [num_pages][page_size][H_kv][D] (bf16 / e4m3)
 // or [num_pages][page_size][1][656].
 //
 // The work is a scatter of a few hundred bytes per request, HBM / latency
@@ -73,12 +75,67 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return c;
 }
 
+// The reciprocal of a scale and whether Markstein's correction applies to it:
+// y = RN(1 / s) (correctly rounded), for scales in [2^-100, 2^100], where
+// neither the reciprocal nor the residual below leaves the normal range.
+struct Recip {
+    float s, y;
+    bool ok;
+};
+__device__ __forceinline__ Recip recip_of(float s) {
+    const float a = fabsf(s);
+    return Recip{s, __frcp_rn(s), a >= 0x1p-100f && a <= 0x1p100f};
+}
+
+// RN(x / s), the quotient rounded to nearest, by Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Develop. 34 (1990)): with y = RN(1/s),
+// q0 = RN(x y) is within an ulp of x / s, the residual r = x - q0 s is exact
+// in one fused multiply-add, and RN(q0 + r y) is the rounded quotient. That
+// equality was checked exhaustively over every finite bf16 x with |x| >= 2^-100
+// and |x / s| in [2^-12, 2^10] for 5090 scales (powers of two and their
+// neighbours, log-uniform 1e-4 .. 1e2, amax / 448): the range in which the
+// e4m3 code depends on the quotient's value (below it the code is a signed
+// zero, above it saturates). Any other input takes the IEEE division.
+// Sets q = RN(x / s); returns false where the correction does not apply.
+__device__ __forceinline__ bool quot_fast(float x, const Recip &d, float &q) {
+    const float q0 = x * d.y;
+    const float r = fmaf(-q0, d.s, x);
+    q = fmaf(r, d.y, q0);
+    const float aq = fabsf(q0);
+    return d.ok && fabsf(x) >= 0x1p-100f && aq >= 0x1p-12f && aq <= 0x1p10f;
+}
+
+// n values / s -> RN quotients; the division runs only where some active lane
+// of the warp has a value outside the correction's range (the vote is over the
+// lanes that reach it: requests that are skipped leave the loop first).
+template <int N>
+__device__ __forceinline__ void quot_rn(const float (&x)[N], const Recip &d, float (&q)[N]) {
+    bool all = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) all &= quot_fast(x[i], d, q[i]);
+    if (!__all_sync(__activemask(), all)) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            float t;
+            if (!quot_fast(x[i], d, t)) q[i] = __fdiv_rn(x[i], d.s);
+        }
+    }
+}
+
 // Eight bf16 values (one 16-byte vector) / s -> eight e4m3 codes.
-__device__ __forceinline__ uint2 quant8(uint4 x, float s) {
+__device__ __forceinline__ uint2 quant8(uint4 x, const Recip &d) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    float v[8], q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
+    }
+    quot_rn(v, d, q);
     uint32_t c[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+    for (int i = 0; i < 4; ++i) c[i] = e4m3x2(q[2 * i], q[2 * i + 1]);
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
@@ -99,39 +156,107 @@ __device__ __forceinline__ int64_t slot_of(const AppendParams &p, int b, bool re
     return (int64_t)page * p.page_size + t % p.page_size;
 }
 
-// bf16 / e4m3 pools. Work item = one 16-byte vector of 8 values at the same
-// place in K and in V of one request (items of a request are consecutive).
-// The two row loads are issued before the position and page lookups, so the
-// three latencies overlap.
-template <bool kFp8>
+// bf16 / e4m3 pools. Work item = kV values (one or two 16-byte vectors of 8)
+// at the same place in K and in V of one request (items of a request are
+// consecutive). The row loads are issued before the position and page
+// lookups, so their latencies overlap. The e4m3 build takes 16 values per item
+// (D a multiple of 16): each thread then moves as many bytes per lookup chain
+// as a bf16 thread, and stores its 16 codes as one 16-byte vector.
+template <bool kFp8, int kV>
 __global__ void __launch_bounds__(kThreads) append_gqa_kernel(const AppendParams p) {
     pdl_wait();               // positions, block table and new rows may come from the previous kernel
     pdl_launch_dependents();  // the next kernel waits for this grid before it reads the pool
-    const int vpr = p.D >> 3;
+    constexpr int NV = kV / 8;  // 16-byte input vectors per item
+    const int vpr = p.D / kV;
     const int per_req = p.H_kv * vpr;
     const int64_t total = (int64_t)p.B * per_req;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
         const int b = (int)(i / per_req);
         const int e = (int)(i - (int64_t)b * per_req);
-        const int64_t src = (int64_t)b * p.row_stride + (int64_t)e * 8;
-        const uint4 xk = ld_stream_v4(p.k_new + src);
-        const uint4 xv = ld_stream_v4(p.v_new + src);
+        const int64_t src = (int64_t)b * p.row_stride + (int64_t)e * kV;
+        uint4 xk[NV], xv[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            xk[j] = ld_stream_v4(p.k_new + src + 8 * j);
+            xv[j] = ld_stream_v4(p.v_new + src + 8 * j);
+        }
         const int64_t slot = slot_of(p, b, e == 0);
         if (slot < 0) continue;
         const int64_t vec = slot * per_req + e;
         if constexpr (!kFp8) {
-            st_v4(p.k_pool + vec * 16, xk);
-            st_v4(p.v_pool + vec * 16, xv);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                st_v4(p.k_pool + vec * kV * 2 + 16 * j, xk[j]);
+                st_v4(p.v_pool + vec * kV * 2 + 16 * j, xv[j]);
+            }
         } else {
             const int h = e / vpr;
-            st_v2(p.k_pool + vec * 8, quant8(xk, __ldg(p.k_scale + h)));
-            st_v2(p.v_pool + vec * 8, quant8(xv, __ldg(p.v_scale + h)));
+            const Recip dk = recip_of(__ldg(p.k_scale + h)), dv = recip_of(__ldg(p.v_scale + h));
+            if constexpr (NV == 2) {
+                const uint2 k0 = quant8(xk[0], dk), k1 = quant8(xk[1], dk);
+                const uint2 v0 = quant8(xv[0], dv), v1 = quant8(xv[1], dv);
+                st_v4(p.k_pool + vec * kV, make_uint4(k0.x, k0.y, k1.x, k1.y));
+                st_v4(p.v_pool + vec * kV, make_uint4(v0.x, v0.y, v1.x, v1.y));
+            } else {
+                st_v2(p.k_pool + vec * kV, quant8(xk[0], dk));
+                st_v2(p.v_pool + vec * kV, quant8(xv[0], dv));
+            }
         }
     }
 }
 
 // 656-byte latent tokens, one warp per request. Lane l holds NoPE values
 // [16l, 16l+16); lanes 8k..8k+7 form block k.
+struct LatentIn {
+    uint4 a0, a1, rope;
+};
+__device__ __forceinline__ LatentIn latent_load(const AppendParams &p, int b, int lane) {
+    const uint16_t *src = p.k_new + (int64_t)b * p.row_stride;
+    LatentIn x;
+    x.a0 = ld_stream_v4(src + lane * 16);
+    x.a1 = ld_stream_v4(src + lane * 16 + 8);
+    x.rope = lane < 8 ? ld_stream_v4(src + kLatentNope + lane * 8) : make_uint4(0u, 0u, 0u, 0u);
+    return x;
+}
+// every lane of the warp calls this for the same request
+__device__ __forceinline__ void latent_store(const AppendParams &p, int b, int lane, const LatentIn &x) {
+    const int64_t slot = slot_of(p, b, lane == 0);  // uniform over the warp
+    if (slot < 0) return;
+    const uint32_t w[8] = {x.a0.x, x.a0.y, x.a0.z, x.a0.w, x.a1.x, x.a1.y, x.a1.z, x.a1.w};
+    // max |x| by the magnitude bits: exact, and a NaN wins (scale 1 then)
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m = max(m, (w[i] << 16) & 0x7FFFFFFFu);
+        m = max(m, w[i] & 0x7FFF0000u);
+    }
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    const float amax = __uint_as_float(m);
+    const float scale = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+    const Recip d = recip_of(scale);
+    float v[16], q[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
+    }
+    quot_rn(v, d, q);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = e4m3x2(q[4 * i], q[4 * i + 1]) | (e4m3x2(q[4 * i + 2], q[4 * i + 3]) << 16);
+    uint8_t *row = p.k_pool + slot * kLatentRow;
+    st_v4(row + lane * 16, make_uint4(c[0], c[1], c[2], c[3]));
+    const float s1 = __shfl_sync(0xFFFFFFFFu, scale, 8);
+    const float s2 = __shfl_sync(0xFFFFFFFFu, scale, 16);
+    const float s3 = __shfl_sync(0xFFFFFFFFu, scale, 24);
+    if (lane == 0)
+        st_v4(row + kLatentScales,
+              make_uint4(__float_as_uint(scale), __float_as_uint(s1), __float_as_uint(s2), __float_as_uint(s3)));
+    if (lane < 8) st_v4(row + kLatentRope + lane * 16, x.rope);
+}
+
 __global__ void __launch_bounds__(kThreads) append_mla_kernel(const AppendParams p) {
     pdl_wait();
     pdl_launch_dependents();
@@ -139,42 +264,7 @@ __global__ void __launch_bounds__(kThreads) append_mla_kernel(const AppendParams
     constexpr int kWarps = kThreads / 32;
     for (int b = blockIdx.x * kWarps + (threadIdx.x >> 5); b < p.B; b += gridDim.x * kWarps) {
         // the row loads first, then the position and page lookups
-        const uint16_t *src = p.k_new + (int64_t)b * p.row_stride;
-        const uint4 a0 = ld_stream_v4(src + lane * 16);
-        const uint4 a1 = ld_stream_v4(src + lane * 16 + 8);
-        const uint4 rope = lane < 8 ? ld_stream_v4(src + kLatentNope + lane * 8) : make_uint4(0u, 0u, 0u, 0u);
-        const int64_t slot = slot_of(p, b, lane == 0);   // uniform over the warp
-        if (slot < 0) continue;
-        const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        // max |x| by the magnitude bits: exact, and a NaN wins (scale 1 then)
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            m = max(m, (w[i] << 16) & 0x7FFFFFFFu);
-            m = max(m, w[i] & 0x7FFF0000u);
-        }
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        const float amax = __uint_as_float(m);
-        const float scale = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
-        uint32_t c[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = e4m3x2(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
-            const uint32_t hi =
-                e4m3x2(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
-            c[i] = lo | (hi << 16);
-        }
-        uint8_t *row = p.k_pool + slot * kLatentRow;
-        st_v4(row + lane * 16, make_uint4(c[0], c[1], c[2], c[3]));
-        const float s1 = __shfl_sync(0xFFFFFFFFu, scale, 8);
-        const float s2 = __shfl_sync(0xFFFFFFFFu, scale, 16);
-        const float s3 = __shfl_sync(0xFFFFFFFFu, scale, 24);
-        if (lane == 0)
-            st_v4(row + kLatentScales,
-                  make_uint4(__float_as_uint(scale), __float_as_uint(s1), __float_as_uint(s2), __float_as_uint(s3)));
-        if (lane < 8) st_v4(row + kLatentRope + lane * 16, rope);
+        latent_store(p, b, lane, latent_load(p, b, lane));
     }
 }
 
@@ -195,11 +285,14 @@ cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stre
         cfg.gridDim = dim3((unsigned)(blocks < kMaxBlocks ? blocks : kMaxBlocks));
         return cudaLaunchKernelEx(&cfg, append_mla_kernel, p);
     }
-    const int64_t items = (int64_t)p.B * p.H_kv * (p.D / 8);
+    const bool wide = kv_dtype == DA_KV_FP8_PER_TENSOR && p.D % 16 == 0;
+    const int64_t items = (int64_t)p.B * p.H_kv * (p.D / (wide ? 16 : 8));
     const int64_t blocks = (items + kThreads - 1) / kThreads;
     cfg.gridDim = dim3((unsigned)(blocks < kMaxBlocks ? blocks : kMaxBlocks));
-    if (kv_dtype == DA_KV_FP8_PER_TENSOR) return cudaLaunchKernelEx(&cfg, append_gqa_kernel<true>, p);
-    return cudaLaunchKernelEx(&cfg, append_gqa_kernel<false>, p);
+    if (kv_dtype == DA_KV_FP8_PER_TENSOR)
+        return wide ? cudaLaunchKernelEx(&cfg, append_gqa_kernel<true, 16>, p)
+                    : cudaLaunchKernelEx(&cfg, append_gqa_kernel<true, 8>, p);
+    return cudaLaunchKernelEx(&cfg, append_gqa_kernel<false, 8>, p);
 }
 
 }  // namespace da
