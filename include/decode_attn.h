@@ -59,10 +59,9 @@ typedef enum {
      * section "数据加载"): 512 e4m3, 4 fp32 scales (one per 128 values), 64 bf16
      * RoPE values. K = the 576 dequantised values, V = the first 512. v_pool
      * must be NULL or equal to k_pool; H_kv = 1, D_qk = 576, D_v = 512.
-     * Input contract: the e4m3 bytes of a token the call reads hold finite
-     * codes (what the quantiser, decode_attn_append_kv, writes: it saturates
-     * at +-448 and never emits 0x7F / 0xFF). The decoder widens codes by bit
-     * moves, which read 0x7F / 0xFF as +-480 rather than NaN. */
+     * Codes 0x7F / 0xFF decode to NaN (and so poison the rows that read
+     * them), as in the bf16 and per-tensor formats; the quantiser,
+     * decode_attn_append_kv, never writes them: it saturates at +-448. */
     DA_KV_FP8_MLA656 = 2
 } da_kv_dtype;
 
@@ -110,9 +109,7 @@ typedef struct {
  * Size in bytes of the sched_meta buffer for this desc (host only, no CUDA
  * call except an SM-count query when desc->num_sms is 0). The buffer holds the
  * scheduling metadata, the split-KV partials (fp32 o and lse per split and
- * output row: query token x query head), the device error word and, for DA_KV_FP8_MLA656, the slots in
- * which the two CTAs of a part swap their partial scores (32 KB per CTA;
- * rewritten by every decode_attn_fwd, never read across calls).
+ * output row: query token x query head) and the device error word.
  */
 int decode_attn_sched_meta_bytes(const da_desc *desc, size_t *bytes);
 
@@ -169,8 +166,9 @@ int decode_attn_sched_meta(const da_desc *desc, const int32_t *cache_seqlens,
  * last s_q tokens are already in the pool (L_b counts them) and draft token
  * j < s_q sees the first L_b - s_q + 1 + j tokens -- the history and the
  * drafts up to itself. A row that sees no token gets out = 0, lse = -inf.
- * Supported: s_q <= 4 for the bf16 and e4m3 formats; the 656-byte format
- * takes s_q = 1. The rows of q, out and lse below are
+ * Supported: s_q <= 4 for all three formats (on the 656-byte format the
+ * sliding window and, when s_q > 1, sparse decode are not offered:
+ * DA_ERR_UNSUPPORTED). The rows of q, out and lse below are
  * then [B][s_q][H_kv*G]; the scheduling metadata must be built with the same s_q.
  *
  * Sliding window (desc->window = W > 0; XQA page, section

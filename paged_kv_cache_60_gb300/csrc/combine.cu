@@ -43,9 +43,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Co
     const float *lp = p.meta.lse_part + (size_t)so * p.rows + hq;
     // lane s holds split s's lse (splits beyond 32 are folded in a loop)
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, lp[(size_t)s * p.rows]);
+    for (int s = lane; s < ns; s += 32) M = fmax_nan(M, lp[(size_t)s * p.rows]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int off = 16; off > 0; off >>= 1) M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, off));
     __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)b * p.rows + hq) * DV;
     float acc[PER_LANE];
 #pragma unroll

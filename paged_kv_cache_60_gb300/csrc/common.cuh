@@ -22,8 +22,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ln(e^a + e^b), -inf when both are -inf
+// max(a, b) that is NaN when either is (fmaxf returns the other operand): a
+// NaN partial -- a NaN code in the pool -- then reaches the merged result
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
 __device__ __forceinline__ float log_add_exp(float a, float b) {
-    const float m = fmaxf(a, b);
+    const float m = fmax_nan(a, b);
     return m == -INFINITY ? -INFINITY : m + log1pf(expf(-fabsf(a - b)));
 }
 

@@ -149,7 +149,7 @@ __device__ __noinline__ void cluster_merge(const MergeArgs p, float *xo, float *
                 ov[q] = q < S ? ld_cluster_f32(mapa_shared(xo_s + 4u * ((uint32_t)r * D + d), (uint32_t)q)) : 0.f;
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) M = fmaxf(M, ls[q]);
+            for (int q = 0; q < 8; ++q) M = fmax_nan(M, ls[q]);
             float acc = 0.f, lse_v = -INFINITY;
             if (M != -INFINITY) {
                 float Z = 0.f;
@@ -666,13 +666,14 @@ __global__ void __launch_bounds__(GqaCfg<D, FP8, NQ, WPC>::THREADS, GqaCfg<D, FP
                     }
                     // lse over the tokens; a request with a single split gets its
                     // attention sink here (the combine adds it to the others)
-                    float lse_v = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -INFINITY, fac = 1.f;
+                    // (a NaN sum -- a NaN code in a row -- stays NaN rather than reading as empty)
+                    float lse_v = !(Ls <= 0.f) ? (M + log2f(Ls)) * kLn2 : -INFINITY, fac = 1.f;
                     if (direct && p.sinks != nullptr) {
                         const float tot = log_add_exp(lse_v, p.sinks[h * C::G + g]);
                         fac = (lse_v == -INFINITY) ? 0.f : expf(lse_v - tot);
                         lse_v = tot;
                     }
-                    sm_fin[g] = (Ls > 0.f) ? vscale * fac / Ls : 0.f;  // out = u * this
+                    sm_fin[g] = !(Ls <= 0.f) ? vscale * fac / Ls : 0.f;  // out = u * this
                     sm_fin[2 * C::G + g] = lse_v;
                 }
                 named_barrier_sync(1, C::NCW * 32);
