@@ -61,8 +61,8 @@ constexpr int KSL = NSL - VSL;              // the other five, read by Q K^T onl
 constexpr int VSLOT = VSL * SLICE;          // 32 KB
 constexpr int KSLOT = KSL * SLICE;          // 40 KB
 constexpr int NR = 2;                       // slots per ring
-constexpr int QTM = 5;                      // q slices in tensor memory: dims [0, 320)
-constexpr int QSM = NSL - QTM;              // q slices in shared memory: dims [320, 576)
+constexpr int QTM = 5;                      // q slices in tensor memory (rank 0: dims [0, 320); rank 1: [256, 576))
+constexpr int QSM = NSL - QTM;              // q slices in shared memory (rank 0: [320, 576); rank 1: [0, 256))
 constexpr int KU = 24;                      // 16-byte units of a row that only Q K^T reads: 16 NoPE + 8 RoPE
 constexpr int VU = 16;                      // NoPE units of the value dims of one CTA
 constexpr int DQ_WARPS = 8, DQ_THREADS = DQ_WARPS * 32;
@@ -84,7 +84,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 0;               // O: 256 fp32 value dims
 constexpr uint32_t S_COL = 256;             // S: 64 fp32 tokens
 constexpr uint32_t P_COL = 320;             // P: 64 bf16 tokens, two per column (32 columns)
-constexpr uint32_t Q_COL = 352;             // q dims [0, 320): two bf16 per column (160 columns)
+constexpr uint32_t Q_COL = 352;             // q slices in tensor memory: two bf16 per column (160 columns)
 constexpr float RESCALE_LOG2 = 8.f;         // re-base the max when it grows by more than 2^8
 static_assert(KUPT * DQ_THREADS == kChunk * KU && VUPT * DQ_THREADS == kChunk * VU, "units per chunk");
 static_assert(Q_COL + QTM * 32 == TMEM_COLS, "tensor memory budget");
@@ -137,7 +137,8 @@ __device__ __forceinline__ bool is_v_slice(int s, int r) { return (s >> 2) == r 
 __device__ __forceinline__ int k_slot_index(int s, int r) { return r == 0 ? s - 4 : (s < 4 ? s : 4); }
 
 // S = Q K^T for one chunk on CTA rank R: the five K-only slices first, then the
-// four value slices (q slices below QTM from tensor memory, the others from
+// four value slices (the q slices of this rank's value dims and one more from
+// tensor memory, the others from
 // shared memory); KONLY selects the K-only or the value group.
 template <int R, bool KONLY>
 __device__ __forceinline__ void mla_issue_qk(uint32_t tmem, uint64_t dq0, uint64_t dslot) {
@@ -148,13 +149,16 @@ __device__ __forceinline__ void mla_issue_qk(uint32_t tmem, uint64_t dq0, uint64
         const int s = KONLY ? (R == 0 ? 4 + k : (k < 4 ? k : 8)) : 4 * R + k;
         const uint64_t db = dslot + (uint64_t)((k * SLICE) >> 4);
         // a 16-dim step advances both descriptors by 32 bytes (2 units of 16 bytes)
-        if (s < QTM) {
-            const uint32_t a = tmem + Q_COL + 32 * s;
+        // rank 0 keeps q slices 0-4 in tensor memory, rank 1 slices 4-8: either way
+        // the value slices, whose MMAs wait on the last tile of a chunk, read q
+        // from tensor memory
+        if (R == 0 ? s < QTM : s >= NSL - QTM) {
+            const uint32_t a = tmem + Q_COL + 32 * (R == 0 ? s : s - (NSL - QTM));
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 umma_bf16_tmem_a_w(tmem + S_COL, a + 8 * i, db + 2 * i, IDESC_QK, !(KONLY && k == 0 && i == 0));
         } else {
-            const uint64_t da = dq0 + (uint64_t)(((s - QTM) * QSLICE) >> 4);
+            const uint64_t da = dq0 + (uint64_t)(((R == 0 ? s - QTM : s) * QSLICE) >> 4);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 umma_bf16_ss_w(tmem + S_COL, da + 2 * i, db + 2 * i, IDESC_QK, !(KONLY && k == 0 && i == 0));
@@ -608,18 +612,20 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 if (r == 0 && (direct || split_ok)) *lse_dst = -INFINITY;
                 continue;
             }
-            // this head's q row of query token `draft`: dims [0, 320) into tensor memory
-            // (the A operand of its first five slices), dims [320, 576) into shared memory
+            // this head's q row of query token `draft`: five slices into tensor memory
+            // (rank 0: dims [0, 320), rank 1: [256, 576)), the other four into shared
+            // memory (rank 0: [320, 576), rank 1: [0, 256)); qs counts 16-byte chunks
             if (!(ok = mbar_wait_warp_ool(qfree, (nseg & 1) ^ 1, abort_flag, p.wait_limit_ns))) break;
             {
                 const uint4 *qs = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.q) +
                                                                  ((size_t)sg.b * rows + draft * HQ + head) * DQK);
+                const int tm0 = r == 0 ? 0 : 32, sm0 = r == 0 ? 40 : 0;
 #pragma unroll 1
                 for (int j = 0; j < 10; ++j) {  // 32 dims = 16 columns per store
                     uint32_t rr[16];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint4 v = qs[4 * j + k];
+                        const uint4 v = qs[tm0 + 4 * j + k];
                         rr[4 * k] = v.x;
                         rr[4 * k + 1] = v.y;
                         rr[4 * k + 2] = v.z;
@@ -629,7 +635,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 }
 #pragma unroll 4
                 for (int k = 0; k < QSM * 8; ++k)  // 16-byte chunk k % 8 of slice k / 8
-                    *reinterpret_cast<uint4 *>(smem + OFF_Q + (k >> 3) * QSLICE + swz(head, k & 7)) = qs[40 + k];
+                    *reinterpret_cast<uint4 *>(smem + OFF_Q + (k >> 3) * QSLICE + swz(head, k & 7)) = qs[sm0 + k];
                 tmem_wait_st();
             }
             fence_proxy_async_smem();
