@@ -217,11 +217,11 @@ __device__ __noinline__ void mla_issue(const MlaParams &p, uint8_t *smem, uint32
             if (!wait(&kfull[slot], par) || !wait(sfree, (cur & 1) ^ 1)) break;
             tc_fence_after();
             mla_issue_qk<R, true>(tmem, dq0, dk0 + (uint64_t)((slot * KSLOT) >> 4));
+            umma_commit_w(&kempty[slot]);  // the K-only slot is free once these have read it
             if (!wait(&vfull[slot], par)) break;
             tc_fence_after();
             mla_issue_qk<R, false>(tmem, dq0, dv0 + (uint64_t)((slot * VSLOT) >> 4));
             umma_commit_w(sfull);
-            umma_commit_w(&kempty[slot]);
             if (c == n - 1) umma_commit_w(qfree);  // q may be replaced once these complete
             if (pend >= 0) issue_pv(pend, pend_first, pend_last, pend_seg);
             pend = cur;
