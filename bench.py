@@ -219,12 +219,13 @@ class DevCopy:
 
 def append_at_scale(torch, da, spec, stream, hbm_peak, reps=50):
     """decode_attn_append_kv on a large batch of the workload's KV format
-    (16384 requests, or 65536 latent tokens), one page of 16 slots per
+    (65536 requests, or 262144 latent tokens: 0.2-0.5 GB moved per call, so
+    that launch and tail costs are a small share), one page of 16 slots per
     request, new rows rotating over enough copies to exceed 2x L2: the append
     kernel's HBM roofline, which decode batch sizes are too small to show."""
     P = 16
     mla = spec.kv_dtype == da.KV_MLA656
-    B = 65536 if mla else 16384
+    B = 262144 if mla else 65536
     H, D = (1, 576) if mla else (spec.H_kv, spec.D_qk)
     g = torch.Generator(device="cuda").manual_seed(spec.seed + 3)
     desc = da.Desc.make(B=B, H_kv=H, G=spec.G, D_qk=D, D_v=spec.D_v, page_size=P, max_pages_per_seq=1,

@@ -65,62 +65,81 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Two fp32 values -> two e4m3 codes (lo in bits 0..7, hi in bits 8..15):
-// round to nearest even, finite results saturate at +-448, NaN -> 0x7F.
+// round to nearest even, finite results saturate at +-448, NaN -> 0x7F (one
+// test per pair on the common path: the sum of two values is NaN when either
+// is).
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     uint32_t c = r;
-    if (lo != lo) c = (c & 0xFF00u) | 0x7Fu;
-    if (hi != hi) c = (c & 0x00FFu) | 0x7F00u;
+    const float t = lo + hi;
+    if (t != t) {
+        if (lo != lo) c = (c & 0xFF00u) | 0x7Fu;
+        if (hi != hi) c = (c & 0x00FFu) | 0x7F00u;
+    }
     return c;
 }
 
 // The reciprocal of a scale and whether Markstein's correction applies to it:
-// y = RN(1 / s) (correctly rounded), for scales in [2^-100, 2^100], where
-// neither the reciprocal nor the residual below leaves the normal range.
+// y = RN(1 / s) (correctly rounded), for scales in [2^-80, 2^100]: the
+// reciprocal stays normal, and an input small enough for the residual below to
+// underflow (|x| < 2^-100) gives |x / s| < 2^-20, which codes to a signed zero
+// whatever its last bit.
 struct Recip {
     float s, y;
     bool ok;
 };
 __device__ __forceinline__ Recip recip_of(float s) {
     const float a = fabsf(s);
-    return Recip{s, __frcp_rn(s), a >= 0x1p-100f && a <= 0x1p100f};
+    return Recip{s, __frcp_rn(s), a >= 0x1p-80f && a <= 0x1p100f};
 }
 
 // RN(x / s), the quotient rounded to nearest, by Markstein's correction
 // (P. Markstein, "Computation of elementary functions on the IBM RISC
 // System/6000 processor", IBM J. Res. Develop. 34 (1990)): with y = RN(1/s),
 // q0 = RN(x y) is within an ulp of x / s, the residual r = x - q0 s is exact
-// in one fused multiply-add, and RN(q0 + r y) is the rounded quotient. That
-// equality was checked exhaustively over every finite bf16 x with |x| >= 2^-100
-// and |x / s| in [2^-12, 2^10] for 5090 scales (powers of two and their
-// neighbours, log-uniform 1e-4 .. 1e2, amax / 448): the range in which the
-// e4m3 code depends on the quotient's value (below it the code is a signed
-// zero, above it saturates). Any other input takes the IEEE division.
-// Sets q = RN(x / s); returns false where the correction does not apply.
-__device__ __forceinline__ bool quot_fast(float x, const Recip &d, float &q) {
-    const float q0 = x * d.y;
-    const float r = fmaf(-q0, d.s, x);
-    q = fmaf(r, d.y, q0);
-    const float aq = fabsf(q0);
-    return d.ok && fabsf(x) >= 0x1p-100f && aq >= 0x1p-12f && aq <= 0x1p10f;
-}
-
-// n values / s -> RN quotients; the division runs only where some active lane
-// of the warp has a value outside the correction's range (the vote is over the
-// lanes that reach it: requests that are skipped leave the loop first).
+// in one fused multiply-add, and RN(q0 + r y) is the rounded quotient, as long
+// as nothing overflows or underflows on the way. That equality was checked
+// exhaustively over every finite bf16 x with |x| >= 2^-100 and |x / s| in
+// [2^-12, 2^10] for 5090 scales (powers of two and their neighbours,
+// log-uniform 1e-4 .. 1e2, amax / 448): the range in which the e4m3 code
+// depends on the quotient's value. Below it the code is a signed zero (the
+// sign is taken from q0, so -0 stays -0), above it the code saturates, and a
+// NaN input gives a NaN quotient, so those need no test. What does: a scale
+// outside the range recip_of accepts, an infinite input, and a quotient large
+// enough to overflow the residual (|x| y >= 2^100): one running max of |x| per
+// group of values tells, and the IEEE division runs only where some active
+// lane of the warp has such a value (the vote is over the lanes that reach it:
+// requests that are skipped leave the loop first).
 template <int N>
 __device__ __forceinline__ void quot_rn(const float (&x)[N], const Recip &d, float (&q)[N]) {
-    bool all = true;
+    float mx = 0.f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) all &= quot_fast(x[i], d, q[i]);
-    if (!__all_sync(__activemask(), all)) {
+    for (int i = 0; i < N; ++i) {
+        const float q0 = x[i] * d.y;
+        const float r = fmaf(-q0, d.s, x[i]);
+        q[i] = copysignf(fmaf(r, d.y, q0), q0);
+        mx = fmaxf(mx, fabsf(x[i]));
+    }
+    const bool fast = d.ok && mx < INFINITY && mx * fabsf(d.y) < 0x1p100f;
+    if (!__all_sync(__activemask(), fast)) {
+        if (!fast) {
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            float t;
-            if (!quot_fast(x[i], d, t)) q[i] = __fdiv_rn(x[i], d.s);
+            for (int i = 0; i < N; ++i) q[i] = __fdiv_rn(x[i], d.s);
         }
     }
+}
+
+// RN(a / 448), the block scale of the 656-byte token, by the same correction
+// with the constant y = RN(1/448); checked exhaustively against the IEEE
+// division for every bf16 magnitude >= 2^-100 (the block maxima are bf16
+// values). Smaller, infinite or NaN maxima take the division.
+__device__ __forceinline__ float div448(float a) {
+    constexpr float y = 0x1.24924ap-9f;  // RN(1 / 448)
+    if (!(a >= 0x1p-100f && a < INFINITY)) return __fdiv_rn(a, kE4m3Max);
+    const float q0 = a * y;
+    const float r = fmaf(-q0, kE4m3Max, a);
+    return fmaf(r, y, q0);
 }
 
 // Eight bf16 values (one 16-byte vector) / s -> eight e4m3 codes.
@@ -162,8 +181,12 @@ __device__ __forceinline__ int64_t slot_of(const AppendParams &p, int b, bool re
 // lookups, so their latencies overlap. The e4m3 build takes 16 values per item
 // (D a multiple of 16): each thread then moves as many bytes per lookup chain
 // as a bf16 thread, and stores its 16 codes as one 16-byte vector.
+// Six blocks per SM (at most 40 registers a thread): the latency of a work
+// item's chain (row loads, position and page lookups, quotients, stores)
+// is hidden by more resident threads; measured faster than the four blocks
+// that 52 registers allow, despite a few spilled words.
 template <bool kFp8, int kV>
-__global__ void __launch_bounds__(kThreads) append_gqa_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kThreads, 6) append_gqa_kernel(const AppendParams p) {
     pdl_wait();               // positions, block table and new rows may come from the previous kernel
     pdl_launch_dependents();  // the next kernel waits for this grid before it reads the pool
     constexpr int NV = kV / 8;  // 16-byte input vectors per item
@@ -234,7 +257,7 @@ __device__ __forceinline__ void latent_store(const AppendParams &p, int b, int l
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
     const float amax = __uint_as_float(m);
-    const float scale = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+    const float scale = amax > 0.f ? div448(amax) : 1.f;
     const Recip d = recip_of(scale);
     float v[16], q[16];
 #pragma unroll
@@ -257,7 +280,7 @@ __device__ __forceinline__ void latent_store(const AppendParams &p, int b, int l
     if (lane < 8) st_v4(row + kLatentRope + lane * 16, x.rope);
 }
 
-__global__ void __launch_bounds__(kThreads) append_mla_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kThreads, 6) append_mla_kernel(const AppendParams p) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
