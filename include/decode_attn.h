@@ -77,7 +77,10 @@ typedef struct {
     int32_t num_pages;         /* pages in the pool */
     int32_t kv_dtype;          /* da_kv_dtype */
     int32_t splits;            /* 0: balanced over the SMs; S > 0: S splits per request */
-    int32_t num_sms;           /* 0: query the current device */
+    int32_t num_sms;           /* 0: query the current device; the automatic partition then counts
+                                  the SMs that can hold the 656-byte kernel's clusters at once, or
+                                  two slots per SM for the bf16 D = 64 build with 3-4 query tokens
+                                  (it runs two CTAs per SM); > 0: the slot count to partition for */
     float softmax_scale;       /* sigma; 0: 1/sqrt(D_qk) */
     int32_t s_q;               /* query tokens per request (0 means 1); see decode_attn_fwd */
     int32_t window;            /* sliding window W in tokens (0: none); see decode_attn_fwd */

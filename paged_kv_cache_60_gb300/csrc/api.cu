@@ -20,6 +20,7 @@ cudaError_t launch_append(int kv_dtype, const AppendParams &p, cudaStream_t stre
 int mla_ctas_per_part(int s_q);
 bool mla_kernel_available();
 int mla_max_parts(int s_q);
+int gqa_ctas_per_sm(int D, bool fp8, int s_q);
 int check_fwd_args(const da_desc *desc, const void *q, const void *k_pool, const void *v_pool,
                    const float *k_scale, const float *v_scale, const int32_t *block_table,
                    const int32_t *cache_seqlens, const void *out, const float *lse, const da_launch_opts *opts);
@@ -92,6 +93,9 @@ int resolve_sms(const da_desc *d, int *nsm) {
         const int clusters = mla_max_parts(sq_of(d));
         if (clusters < 1) return DA_ERR_CUDA;
         if (cpc * clusters < *nsm) *nsm = cpc * clusters;
+    } else {
+        // the GQA builds that run two CTAs per SM count two slots per SM
+        *nsm *= gqa_ctas_per_sm(d->D_qk, d->kv_dtype == DA_KV_FP8_PER_TENSOR, sq_of(d));
     }
     return DA_OK;
 }

@@ -44,6 +44,13 @@ def device_sms() -> int:
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+def auto_slots(spec) -> int:
+    """SM slots the library's automatic partition counts for a GQA workload:
+    the bf16 D = 64 build for three or four query tokens runs two CTAs per SM."""
+    two = spec.kv_dtype == 0 and spec.D_qk == 64 and spec.s_q in (3, 4)
+    return device_sms() * (2 if two else 1)
+
+
 def make_desc(w, splits=None, num_sms=0):
     s = w.spec
     return da.Desc.make(B=s.B, H_kv=s.H_kv, G=s.G, D_qk=s.D_qk, D_v=s.D_v, page_size=s.page_size,

@@ -10,7 +10,9 @@ import oracle
 import paged_kv_cache_60_gb300 as da
 from workloads import WorkloadSpec, make_workload, spec_by_name, KV_BF16, KV_FP8
 
-from gpu_util import LSE_TOL, OUT_TOL, DeviceWorkload, ensure_built, make_desc, max_err, run
+from oracle.sched_ref import sched_ref
+
+from gpu_util import LSE_TOL, OUT_TOL, DeviceWorkload, auto_slots, device_sms, ensure_built, make_desc, max_err, read_meta, run
 
 pytestmark = pytest.mark.gpu
 
@@ -108,3 +110,29 @@ def test_unsupported_s_q_rejected_on_host():
                      s_q=5)
     with pytest.raises(da.DecodeAttnError):
         da.sched_meta_bytes(d)
+
+
+def test_two_ctas_per_sm_partition():
+    """The bf16 D = 64 build for three or four query tokens runs two CTAs per
+    SM: its automatic partition counts two slots per SM, bit-exact against the
+    oracle's partition for that count, and the results still match the oracle."""
+    for s_q in (3, 4):
+        spec = WorkloadSpec(name="t", B=len(LENGTHS), H_kv=2, G=8, D_qk=64, D_v=64, page_size=16, kv_dtype=KV_BF16,
+                            lengths=LENGTHS, splits=0, extra_pages=5, seed=90 + s_q, s_q=s_q)
+        w = make_workload(spec)
+        desc = make_desc(w)
+        assert da.num_parts(desc) == (2 * device_sms()) // spec.H_kv
+        out, lse, meta, desc = run(w)
+        torch.cuda.synchronize()
+        assert da.get_error(meta) == 0
+        got = read_meta(meta, desc)
+        ref = sched_ref(w.lengths, spec.H_kv, 0, num_sms=auto_slots(spec), s_q=s_q)
+        assert got["parts"] == ref.parts
+        assert got["split_offset"] == ref.split_offset
+        ref_out, ref_lse = oracle.attend_multi(w)
+        e_out, e_lse = max_err(out.view(ref_out.shape), lse.view(ref_lse.shape), ref_out, ref_lse)
+        assert e_out <= OUT_TOL and e_lse <= LSE_TOL, (e_out, e_lse)
+    # the other multi-token builds keep one slot per SM
+    spec = WorkloadSpec(name="t", B=2, H_kv=2, G=8, D_qk=128, D_v=128, page_size=16, kv_dtype=KV_BF16,
+                        lengths=[100, 200], splits=0, seed=95, s_q=4)
+    assert da.num_parts(make_desc(make_workload(spec))) == device_sms() // 2

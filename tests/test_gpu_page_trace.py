@@ -15,7 +15,7 @@ import paged_kv_cache_60_gb300 as da
 from oracle.sched_ref import CHUNK, first_chunk, part_segments, sched_ref, window_start
 from workloads import KV_BF16, KV_FP8, KV_MLA656, WorkloadSpec, make_workload
 
-from gpu_util import DeviceWorkload, device_sms, make_desc, debug_build_library
+from gpu_util import DeviceWorkload, auto_slots, device_sms, make_desc, debug_build_library
 
 pytestmark = pytest.mark.gpu
 
@@ -100,7 +100,7 @@ def test_gqa_page_trace_bit_exact(tlib, case):
     w = make_workload(_gqa(**kw))
     s = w.spec
     desc = make_desc(w, num_sms=nsm)
-    ref = sched_ref(w.lengths, s.H_kv, s.splits, nsm or device_sms(), window=s.window, s_q=s.s_q)
+    ref = sched_ref(w.lengths, s.H_kv, s.splits, nsm or auto_slots(s), window=s.window, s_q=s.s_q)
     P = s.page_size
     bt_tok = min(P, CHUNK)
     nb = CHUNK // bt_tok
