@@ -111,15 +111,34 @@ __device__ __forceinline__ Recip recip_of(float s) {
 // group of values tells, and the IEEE division runs only where some active
 // lane of the warp has such a value (the vote is over the lanes that reach it:
 // requests that are skipped leave the loop first).
+// Pairs of values go through the packed fp32 pipe (mul.rn / fma.rn on .f32x2:
+// each lane rounds exactly as the scalar instruction does).
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
 template <int N>
 __device__ __forceinline__ void quot_rn(const float (&x)[N], const Recip &d, float (&q)[N]) {
+    static_assert(N % 2 == 0, "pairs of values");
     float mx = 0.f;
+    const uint64_t y2 = f2pack(d.y, d.y), ns2 = f2pack(-d.s, -d.s);
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const float q0 = x[i] * d.y;
-        const float r = fmaf(-q0, d.s, x[i]);
-        q[i] = copysignf(fmaf(r, d.y, q0), q0);
-        mx = fmaxf(mx, fabsf(x[i]));
+    for (int i = 0; i < N; i += 2) {
+        const uint64_t x2 = f2pack(x[i], x[i + 1]);
+        uint64_t q02, r2, qq2;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q02) : "l"(x2), "l"(y2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r2) : "l"(q02), "l"(ns2), "l"(x2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(qq2) : "l"(r2), "l"(y2), "l"(q02));
+        float q0a, q0b, qa, qb;
+        f2unpack(q02, q0a, q0b);
+        f2unpack(qq2, qa, qb);
+        q[i] = copysignf(qa, q0a);
+        q[i + 1] = copysignf(qb, q0b);
+        mx = fmaxf(mx, fmaxf(fabsf(x[i]), fabsf(x[i + 1])));
     }
     const bool fast = d.ok && mx < INFINITY && mx * fabsf(d.y) < 0x1p100f;
     if (!__all_sync(__activemask(), fast)) {
