@@ -287,8 +287,9 @@ int decode_attn_get_error(const void *sched_meta, int32_t *device_error, cudaStr
  * the library keeps it until the process exits. Problems whose
  * decode_attn_sched_meta_bytes exceeds that size are rejected with
  * DA_ERR_META_SIZE. With the 656-byte format the automatic split count
- * (desc->splits = 0) of a GB300 needs about 20 MB and is rejected: pass a fixed
- * split count or a smaller desc->num_sms. Sparse decode (desc->topk > 0) needs
+ * (desc->splits = 0) of a GB300 needs (76 + B) x 256 KB of partials at s_q = 1,
+ * over 16 MiB for any B, and is rejected: pass a fixed split count or a
+ * smaller desc->num_sms. Sparse decode (desc->topk > 0) needs
  * indices, which this call cannot take: DA_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current): make that first call
