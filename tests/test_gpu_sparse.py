@@ -102,9 +102,10 @@ def test_sparse_schedule_bitexact(splits):
     assert got["num_splits"] == ref.num_splits
 
 
-def test_sparse_bench_workload():
-    """The top-k 2048 workload at full size: all 128 requests against the oracle."""
-    spec = spec_by_name("sparse_mla_topk2048")
+@pytest.mark.parametrize("name", ["sparse_mla_topk2048", "sparse_mla_topk32768"])
+def test_sparse_bench_workload(name):
+    """The top-k workloads at full size: every request against the oracle."""
+    spec = spec_by_name(name)
     w = make_workload(spec)
     out, lse, meta, _ = run(w)
     torch.cuda.synchronize()

@@ -109,6 +109,12 @@ CONFIGS = [
         name="sparse_mla_topk2048", B=128, H_kv=1, G=128, D_qk=576, D_v=512, page_size=64,
         kv_dtype=KV_MLA656, lengths=[8192] * 128, splits=0, seed=1009, topk=2048,
         description="B=128 H_q=128 656-byte FP8 tokens, L=8192, top-k 2048 positions per request"),
+    # the same row's top-k 32768 figure; the page gives neither batch nor context,
+    # so this takes the dense latent workload's batch and a context of twice top-k
+    WorkloadSpec(
+        name="sparse_mla_topk32768", B=32, H_kv=1, G=128, D_qk=576, D_v=512, page_size=64,
+        kv_dtype=KV_MLA656, lengths=[65536] * 32, splits=0, seed=1012, topk=32768,
+        description="B=32 H_q=128 656-byte FP8 tokens, L=65536, top-k 32768 positions per request"),
 ]
 
 
