@@ -180,6 +180,21 @@ def test_append_large_batch(kv_dtype, H_kv, D):
     _check(_case(kv_dtype, 4096, H_kv, D, 8, seed=3, max_pages=1, specials=False))
 
 
+def test_append_extreme_scales():
+    """Per-tensor scales at and beyond the range in which the quotient takes
+    the corrected multiply (2^-80 .. 2^100), and inputs whose quotient would
+    overflow the residual: the codes still equal the oracle's, byte for byte."""
+    c = _case(KV_FP8, 64, 6, 128, 16, seed=13, specials=False)
+    c["ks"] = torch.tensor([2.0 ** -90, 2.0 ** 105, 2.0 ** -79, 1e-30, 2.0 ** 100, 2.0 ** -80], dtype=torch.float32)
+    c["vs"] = torch.tensor([2.0 ** -81, 3.0 ** 60, 1e-24, 2.0 ** 99, 0.75, 2.0 ** -100], dtype=torch.float32)
+    g = torch.Generator().manual_seed(14)
+    mag = torch.tensor([1e-30, 1e-20, 1e-6, 1.0, 1e4, 1e20, 1e30, 3e38])
+    for t in ("k_new", "v_new"):
+        x = torch.randn(c[t].shape, generator=g) * mag[torch.randint(0, len(mag), c[t].shape, generator=g)]
+        c[t] = x.to(torch.bfloat16)
+    _check(c)
+
+
 def test_append_all_skipped_writes_nothing():
     c = _case(KV_FP8, 16, 2, 128, 16, seed=9)
     c["pos"][:] = -1
