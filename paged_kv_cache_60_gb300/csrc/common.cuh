@@ -113,21 +113,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
-// Non-blocking test of phase completion.
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait that ignores the abort flag (for draining work already issued).
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_ns();
@@ -372,12 +357,6 @@ __device__ __forceinline__ bool mbar_wait_warp_cluster(uint64_t *bar, uint32_t p
         }
     }
 }
-// Arrive on another CTA's mbarrier without ordering earlier memory accesses
-// (for acknowledgements whose loads have already been consumed).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
@@ -416,28 +395,11 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, i
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-// tcgen05.mma kind::f16 with the A operand read from tensor memory (rows in lanes,
-// K packed two bf16 per 32-bit column) and B from a shared-memory descriptor.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                                 bool accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-// The same with both operands read from shared-memory descriptors.
-__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                             bool accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-// The two MMAs above and the commit below, issued once for a converged warp:
-// every lane executes the statement, elect.sync picks one to issue it, so the
-// operands may live in warp-uniform registers.
+// tcgen05.mma kind::f16, issued once for a converged warp: every lane executes
+// the statement, elect.sync picks one to issue it, so the operands may live in
+// warp-uniform registers. This one reads the A operand from tensor memory (rows
+// in lanes, K packed two bf16 per 32-bit column) and B from a shared-memory
+// descriptor; the next reads both from shared-memory descriptors.
 __device__ __forceinline__ void umma_bf16_tmem_a_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                    bool accumulate) {
     asm volatile(
@@ -454,16 +416,13 @@ __device__ __forceinline__ void umma_bf16_ss_w(uint32_t d_tmem, uint64_t a, uint
         "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
         : "memory");
 }
+// Arrive once on `bar` when every MMA this thread issued so far has completed
+// (one elected lane of a converged warp).
 __device__ __forceinline__ void umma_commit_w(uint64_t *bar) {
     asm volatile(
         "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
         : "memory");
-}
-// Arrive once on `bar` when every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

@@ -133,7 +133,6 @@ __device__ __forceinline__ void dequant16(const uint4 v, float scale, uint4 &lo,
 
 // Slice s of a latent row in this CTA's rings: the value slot holds slices
 // [4 r, 4 r + 4), the K-only slot the other five in increasing order.
-__device__ __forceinline__ bool is_v_slice(int s, int r) { return (s >> 2) == r && s < 8; }
 __device__ __forceinline__ int k_slot_index(int s, int r) { return r == 0 ? s - 4 : (s < 4 ? s : 4); }
 
 // S = Q K^T for one chunk on CTA rank R: the five K-only slices first, then the
