@@ -436,7 +436,33 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     rows[k] = (in && pg_ok && t0 + tok_of(k) < sg.L) ? rb + tok_of(k) : -1;
             };
             const bool one_page = !SPARSE && p.page_size >= kChunk;
-            int pos2[6], row0[6], row1[6];
+            // Sparse decode: lane l of a warp looks up one of the 16 distinct tokens
+            // the warp's lanes need (lanes l and l + 16 the same one) and the rows
+            // reach the lanes that need them by shuffles: one position, page and row
+            // per lane and chunk, not six (215 vs 277 us per top-k 2048 call). Dense
+            // decode with pages shorter than a chunk keeps one lookup per token and
+            // thread (its pages come from the block-table window by shuffles anyway;
+            // the shared form there cost the dense build 7 % on one-page chunks).
+            const int lk = lane & 15, dw = dt >> 5;
+            const int wtok = lk < 8 ? 2 * dw + (lk & 1) + 16 * (lk >> 1) : 4 * dw + ((lk - 8) & 3) + 32 * ((lk - 8) >> 2);
+            auto src_of = [&](int k) { return k < 4 ? 2 * k + (lane >> 4) : 8 + ((lane >> 3) & 3) + 4 * (k - 4); };
+            auto spread = [&](int r, int(&rows)[6]) {
+#pragma unroll
+                for (int k = 0; k < 6; ++k) rows[k] = __shfl_sync(0xffffffffu, r, src_of(k));
+            };
+#ifdef DA_PAGE_TRACE
+            // test build: the trace value of this lane's token, handed to the lanes that record it
+            auto trace_spread = [&](int t, int pg, int idx) {
+                const int tv = t >= 0 ? pg * p.page_size + t % p.page_size : -2;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int v = __shfl_sync(0xffffffffu, tv, src_of(k));
+                    if (p.page_trace && blockIdx.y == 0 && pf_lane && idx < p.page_trace_cap)
+                        p.page_trace[((size_t)part * p.page_trace_cap + idx) * kChunk + tok_of(k)] = v;
+                }
+            };
+#endif
+            int pos2 = -1, pos2a[6], row0[6], row1[6];  // positions in chunk c + 2: this lane's (sparse), per token (dense)
             // prologue: rows of chunks 0 and 1 (prefetched), positions of chunk 2
             if (one_page) {
                 chunk_rows_dense(0, row0);
@@ -454,6 +480,16 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                     }
                 }
 #endif
+            } else if (SPARSE) {
+                const int t0 = position(0, wtok), t1 = position(1, wtok);
+                const int pg0 = page_of(t0), pg1 = page_of(t1);
+                spread(row_of(t0, pg0), row0);
+                spread(row_of(t1, pg1), row1);
+                pos2 = position(2, wtok);
+#ifdef DA_PAGE_TRACE
+                trace_spread(t0, pg0, cur);
+                if (n > 1) trace_spread(t1, pg1, cur + 1);
+#endif
             } else
 #pragma unroll
             for (int k = 0; k < 6; ++k) {
@@ -461,7 +497,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 const int pg0 = page_of(t0), pg1 = page_of(t1);
                 row0[k] = row_of(t0, pg0);
                 row1[k] = row_of(t1, pg1);
-                pos2[k] = position(2, tok_of(k));
+                pos2a[k] = position(2, tok_of(k));
 #ifdef DA_PAGE_TRACE
                 if (p.page_trace && blockIdx.y == 0 && pf_lane && k < 4) {
                     if (cur < p.page_trace_cap)
@@ -493,10 +529,14 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                 const uint32_t par = ((cur / NR) & 1) ^ 1;
                 // a. block-table lookups of chunk c + 2
                 if (!SPARSE && c + 2 < n) advance(page_index((sg.lc0 + c + 2) * kChunk));
-                int pg2[6];
+                int pg2 = -1, pg2a[6];
                 if (!one_page) {
+                    if (SPARSE) {
+                        pg2 = page_of(pos2);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 6; ++k) pg2[k] = page_of(pos2[k]);
+                        for (int k = 0; k < 6; ++k) pg2a[k] = page_of(pos2a[k]);
+                    }
                 }
                 // b. loads of the value units of chunk c
                 uint4 vn[4];
@@ -526,14 +566,19 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                                 row2[k] >= 0 ? row2[k] : -2;
                     }
 #endif
+                } else if (SPARSE) {
+                    spread(row_of(pos2, pg2), row2);
+#ifdef DA_PAGE_TRACE
+                    if (c + 2 < n) trace_spread(pos2, pg2, cur + 2);
+#endif
                 } else
 #pragma unroll
                 for (int k = 0; k < 6; ++k) {
-                    row2[k] = row_of(pos2[k], pg2[k]);
+                    row2[k] = row_of(pos2a[k], pg2a[k]);
 #ifdef DA_PAGE_TRACE
                     if (p.page_trace && blockIdx.y == 0 && pf_lane && k < 4 && c + 2 < n && cur + 2 < p.page_trace_cap)
                         p.page_trace[((size_t)part * p.page_trace_cap + cur + 2) * kChunk + tok_of(k)] =
-                            pos2[k] >= 0 ? pg2[k] * p.page_size + pos2[k] % p.page_size : -2;
+                            pos2a[k] >= 0 ? pg2a[k] * p.page_size + pos2a[k] % p.page_size : -2;
 #endif
                 }
                 if (!SPARSE && pf_lane) {
@@ -542,8 +587,12 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                         if (row2[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row2[k] * ROW_BYTES, ROW_BYTES);
                 }
                 if (!one_page) {
+                    if (SPARSE) {
+                        pos2 = position(c + 3, wtok);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 6; ++k) pos2[k] = position(c + 3, tok_of(k));
+                        for (int k = 0; k < 6; ++k) pos2a[k] = position(c + 3, tok_of(k));
+                    }
                 }
                 // e. loads of the K-only units of chunk c + 1
 #pragma unroll
