@@ -251,10 +251,6 @@ __device__ __forceinline__ float ldg_stream4f(const void *ptr) {
     return v;
 }
 // Bring `bytes` (a multiple of 16, from a 16-byte aligned address) into L2
-// without waiting: the loads that follow hit L2 instead of HBM.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
     uint32_t y;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));

@@ -318,12 +318,12 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
         // K-only NoPE units, four value units and two RoPE units, the same kind of
         // work on every lane. A warp's loads cover 256 contiguous bytes of two rows.
         // Within a segment the work is software-pipelined: the block-table lookups
-        // of chunk c + 2 (and, dense decode, the L2 prefetch of its rows), the loads of the value
-        // units of chunk c before its K-only units are converted, and the loads of
+        // of chunk c + 2, the loads of the value units of chunk c before its K-only
+        // units are converted, and the loads of
         // the K-only units of chunk c + 1 before the value units of c are.
         const int dt = threadIdx.x - (1 + SM_WARPS) * 32;  // 0 .. 255
         const int gk = 16 * (1 - r) + (dt & 15), gv = 16 * r + (dt & 15), gr = dt & 7;
-        const bool pf_lane = (dt & 15) == 0;               // these 16 threads cover the 64 rows of a chunk
+        const bool pf_lane = (dt & 15) == 0;               // these 16 threads cover the 64 rows of a chunk (page trace)
         auto tok_of = [&](int k) { return k < 4 ? (dt >> 4) + 16 * k : (dt >> 3) + 32 * (k - 4); };
         // Where this thread's units land in a slot: token rows dt / 16 + 16 i share
         // their swizzle (token & 7), so the offsets of the two 16-byte chunks of a
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
             };
 #endif
             int pos2 = -1, pos2a[6], row0[6], row1[6];  // positions in chunk c + 2: this lane's (sparse), per token (dense)
-            // prologue: rows of chunks 0 and 1 (prefetched), positions of chunk 2
+            // prologue: rows of chunks 0 and 1, positions of chunk 2
             if (one_page) {
                 chunk_rows_dense(0, row0);
                 chunk_rows_dense(1, row1);
@@ -508,15 +508,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                             t1 >= 0 ? pg1 * p.page_size + t1 % p.page_size : -2;
                 }
 #endif
-            }
-            // dense decode only: for rows at scattered positions the prefetch
-            // changed neither the time nor the DRAM traffic (measured)
-            if (!SPARSE && pf_lane) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (row0[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row0[k] * ROW_BYTES, ROW_BYTES);
-                    if (row1[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row1[k] * ROW_BYTES, ROW_BYTES);
-                }
             }
             uint4 kn[4], kr[2];
             float ksc[4];
@@ -580,11 +571,6 @@ __global__ void __launch_bounds__(mla::THREADS, 1) mla_decode_kernel(const __gri
                         p.page_trace[((size_t)part * p.page_trace_cap + cur + 2) * kChunk + tok_of(k)] =
                             pos2a[k] >= 0 ? pg2a[k] * p.page_size + pos2a[k] % p.page_size : -2;
 #endif
-                }
-                if (!SPARSE && pf_lane) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (row2[k] >= 0) prefetch_l2_bulk(p.pool + (size_t)row2[k] * ROW_BYTES, ROW_BYTES);
                 }
                 if (!one_page) {
                     if (SPARSE) {
