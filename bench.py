@@ -322,6 +322,14 @@ def oracle_time_per_call(w, budget_s):
 
 
 # ----------------------------------------------------------------------------- arms
+def workload_config(name, w):
+    """The workload's shape, as both arms report it."""
+    spec = w.spec
+    return {"workload": name, "desc": spec.description, "B": spec.B, "s_q": spec.s_q, "window": spec.window,
+            "sinks": spec.sinks, "topk": spec.topk, "H_q": spec.H_q, "H_kv": spec.H_kv, "D_qk": spec.D_qk,
+            "D_v": spec.D_v, "page_size": spec.page_size, "splits": spec.splits, "kv_bytes_per_call": w.kv_bytes()}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -339,7 +347,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "us/call", "n_gpus": args.gpus,
             "steps": len(times), "warmup": args.warmup, "ms_per_step": round(v / 1000.0, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload, "desc": w.spec.description},
+            "data": "synthetic", "config": workload_config(args.workload, w),
             "cpu_baseline": {"value": round(v, 3), "unit": "us/call", "cores": cores, "kind": "oracle",
                              "sample": text},
             "e2e": {"value": round(v, 3), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -604,11 +612,7 @@ def run_ours(args, rank, world, local):
             "dtype": {da.KV_BF16: "bf16", da.KV_FP8: "fp8-e4m3 kv / bf16 q,out"}.get(
                 spec.kv_dtype, "fp8-e4m3 656-byte kv dequantised to bf16 / bf16 q,out"),
             "data": "synthetic",
-            "config": {"workload": args.workload, "desc": spec.description, "B": spec.B, "s_q": spec.s_q,
-                       "window": spec.window, "sinks": spec.sinks, "topk": spec.topk,
-                       "H_q": spec.H_q,
-                       "H_kv": spec.H_kv, "D_qk": spec.D_qk, "D_v": spec.D_v, "page_size": spec.page_size,
-                       "splits": spec.splits, "kv_bytes_per_call": kv_bytes,
+            "config": {**workload_config(args.workload, w),
                        "l2": ("inputs rotate over %d copies (%.0f MB > 2x L2)" % (copies, copies * kv_bytes / 1e6))
                        if copies > 1 else "inputs larger than 2x L2",
                        "launch": "eager" if args.eager else f"cuda graphs of {cpg} calls",
