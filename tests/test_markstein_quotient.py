@@ -1,11 +1,17 @@
 """The append kernels compute x / s as Markstein's correction of the
 reciprocal product (P. Markstein, IBM J. Res. Develop. 34, 1990): y = RN(1/s),
-q0 = RN(x y), r = RN(x - q0 s) (exact), q = RN(q0 + r y). They take that path
-only for |x| >= 2^-100, |q0| in [2^-12, 2^10] and s in [2^-100, 2^100], where it
-must equal the IEEE quotient RN(x / s) -- the value the e4m3 encoder of the
-oracle uses. Checked here in exact arithmetic on every finite bf16 x for a
-sample of scales (powers of two and their neighbours, log-uniform, amax/448).
-CPU only: it pins the identity the GPU path relies on, not the GPU."""
+q0 = RN(x y), r = RN(x - q0 s) (exact), q = RN(q0 + r y), with the sign of q0
+put on q (so that -0 stays -0). They take that path for a scale in
+[2^-80, 2^100] and a group of finite inputs whose largest |x| y stays below
+2^100; the IEEE division elsewhere. Two facts make that exact for the e4m3
+codes the oracle computes from RN(x / s): where the code depends on the
+quotient's last bit (|x / s| in [2^-12, 2^10]) the corrected quotient equals
+RN(x / s), checked in exact arithmetic on every finite bf16 x for a sample of
+scales (powers of two and their neighbours, log-uniform, amax/448); and
+everywhere on the fast path the code of the corrected quotient equals the
+code of RN(x / s), checked over every finite bf16 x for scales across the
+whole accepted range. CPU only: these pin the identities the GPU path relies
+on, not the GPU."""
 from fractions import Fraction
 
 import numpy as np
@@ -52,3 +58,34 @@ def test_markstein_quotient_equals_ieee_division_where_used():
             assert np.array_equal(q[used], (x / s)[used]), float(s)
             checked += int(used.sum())
     assert checked > 500_000
+
+
+def _corrected(x, s):
+    """The kernels' fast path for the values x (float32) and the scale s."""
+    x64 = x.astype(np.float64)
+    y = np.float32(1.0) / s                                        # RN(1 / s)
+    q0 = x * y                                                     # RN(x y)
+    r = (x64 - q0.astype(np.float64) * np.float64(s)).astype(np.float32)  # RN(x - q0 s)
+    q = _rn32_sum(r.astype(np.float64) * np.float64(y), q0.astype(np.float64))
+    return np.copysign(q, q0), y
+
+
+def test_corrected_quotient_gives_the_oracles_codes_on_the_whole_fast_path():
+    from oracle.append_ref import e4m3_encode
+    rng = np.random.default_rng(11)
+    x = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    x = x[np.isfinite(x)]                                          # every finite bf16, both zeros included
+    p2 = np.float32(2.0) ** np.arange(-80, 101, 9, dtype=np.float32)
+    scales = np.concatenate([p2, np.nextafter(p2, np.float32(np.inf)),
+                             np.float32(2.0) ** rng.uniform(-80, 100, 24).astype(np.float32),
+                             np.float32([2.0 ** -80, 2.0 ** 100, 0.0137, 1.0 / 448, 3.0 ** 60])])
+    checked = 0
+    with np.errstate(all="ignore"):
+        for s in scales:
+            s = np.float32(s)
+            q, y = _corrected(x, s)
+            fast = np.abs(x).astype(np.float64) * abs(float(y)) < 2.0 ** 100
+            got, want = e4m3_encode(q[fast]), e4m3_encode((x / s)[fast])
+            assert np.array_equal(got, want), (float(s), x[fast][got != want][:4])
+            checked += int(fast.sum())
+    assert checked > 3_000_000
